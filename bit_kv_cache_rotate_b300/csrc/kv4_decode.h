@@ -1,0 +1,41 @@
+// kv4_decode.h -- internal interface between the host API and the decode
+// kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kv4 {
+
+struct DecodeArgs {
+  const uint16_t* q;       // bf16 [B][T][Hq][D], unrotated
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;  // latent: == k_cache, read with the K layout
+  const float* k_scale;    // fp8 only
+  const float* v_scale;    // fp8 only
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* part_o;           // [B][T][Hq][S][D]
+  float* part_lse;         // [B][T][Hq][S]
+  int32_t* dev_error;
+  int B, T, Hq, Hkv, max_pages, num_pages, S;
+  int latent;
+  float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
+};
+
+// Splits per sequence: enough CTAs to fill every SM a few times over, never
+// more splits than pages.
+inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
+  (void)head_dim;
+  const int target = 2 * sms;
+  int s = (target + units - 1) / units;
+  if (s > max_pages) s = max_pages;
+  if (s > 256) s = 256;
+  return s < 1 ? 1 : s;
+}
+
+cudaError_t launch_decode_ref(bool fp8, int D, const DecodeArgs& a, cudaStream_t st);
+bool fast_path_supported(int D, int G, int T, bool latent);
+cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st);
+
+}  // namespace kv4

@@ -1,0 +1,195 @@
+/*
+ * kv4.h -- C ABI of libkv4: 4-bit rotated KV-cache decode attention on B300.
+ *
+ * The method is the one described on the "UltraQuant on AMD Instinct" page:
+ *   section "What is UltraQuant"  -- every key/value head vector is rotated by
+ *     a Walsh-Hadamard transform, then stored as FP4 (E2M1) codes with one
+ *     shared power-of-two (UE8M0) scale per 32 channels: 17 bytes per 32
+ *     values instead of 32 for an 8-bit cache; the attention kernel consumes
+ *     the FP4 codes directly and applies the power-of-two scale as part of the
+ *     multiply, with no lookup-table dequantisation;
+ *   section "Why UltraQuant beats 8-bit KV" -- each decode step re-reads the
+ *     whole cache, so the step time follows the cache bytes;
+ *   section "Throughput-latency trade-off" -- MTP verify: several query
+ *     positions of one sequence share one paged cache, causal among them.
+ *
+ * Conventions for every entry point
+ *   - Pointers marked "device" are device (HBM) pointers owned by the caller;
+ *     the library never allocates, frees or synchronises.  All work is queued
+ *     on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Host-side validation runs first and returns KV4_ERR_INVALID_ARG or
+ *     KV4_ERR_UNSUPPORTED without launching anything.  A failed launch returns
+ *     KV4_ERR_CUDA.  Errors found on the device (a page id outside
+ *     [0, num_pages), a context length outside [q_per_seq, max_pages *
+ *     page_size], a slot outside the cache) skip the offending work and set
+ *     *dev_error to a nonzero KV4_DEVERR_* bit when dev_error is non-NULL; the
+ *     caller reads it after synchronising.  No kernel traps or waits on
+ *     another block.
+ *   - Supported: head_dim in {64, 128, 256, 512}; page_size 16; num_q_heads a
+ *     multiple of num_kv_heads; q_per_seq (T) in 1..8.
+ *   - Entry points hold no global state and are thread-safe.
+ *
+ * Cache layout (one block per (page, kv head), blocks page-major:
+ * block index = page * num_kv_heads + head, block bytes = P*D/2 + P*D/32):
+ *   K block (also the latent cache):
+ *     codes  [P][D/2]  token-major: byte (t, j) = channel 2j (low nibble),
+ *                      channel 2j+1 (high nibble) of token t
+ *     scales [P][D/32] one UE8M0 byte (exponent + 127) per (token, group)
+ *   V block:
+ *     codes  [D][P/2]  channel-major: byte (d, j) = token 2j (low nibble),
+ *                      token 2j+1 (high nibble) of channel d
+ *     scales [P][D/32] as for K
+ * Codes are OCP E2M1 nibbles (sign | 2 exponent bits | 1 mantissa bit).
+ * Values are stored in the rotated space: y = H_D x with H_D the orthonormal
+ * Sylvester Walsh-Hadamard matrix (natural order); q is rotated by the same
+ * H_D inside the decode call and the output is rotated back, so callers pass
+ * and receive unrotated vectors.
+ */
+#ifndef KV4_H_
+#define KV4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kv4_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  KV4_OK = 0,
+  KV4_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad relation between sizes */
+  KV4_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim, page_size, T) */
+  KV4_ERR_CUDA = 3,          /* a kernel launch failed */
+  KV4_ERR_DEVICE_BOUNDS = 4  /* reserved for callers that fold *dev_error into a status */
+} kv4_status;
+
+/* Bits written to *dev_error by kernels. */
+#define KV4_DEVERR_PAGE 1      /* block_tables entry outside [0, num_pages) */
+#define KV4_DEVERR_CONTEXT 2   /* context_lens[b] outside [q_per_seq, max_pages*page_size] */
+#define KV4_DEVERR_SLOT 4      /* slot_mapping entry outside the cache */
+
+/* Human-readable name of a status. */
+const char* kv4_status_string(kv4_status s);
+
+/* Bytes of one 4-bit cache (K, V or latent): num_pages * num_kv_heads *
+ * (page_size*head_dim/2 + page_size*head_dim/32) -- 17 bytes per 32 values
+ * ("What is UltraQuant").  Returns 0 for invalid sizes. */
+size_t kv4_cache_bytes(int num_pages, int num_kv_heads, int page_size, int head_dim);
+
+/* Quantise-on-append ("What is UltraQuant": rotation, FP4 codes, one
+ * power-of-two scale per 32 channels).
+ *   k, v          device bf16 [num_tokens][num_kv_heads][head_dim], unrotated.
+ *                 v == NULL selects the latent cache (MLA): only k is written,
+ *                 into k_cache, and v_cache must be NULL too.
+ *   slot_mapping  device int32 [num_tokens]: token i goes to page
+ *                 slot/page_size, row slot%page_size; negative slots skip.
+ *   k_cache, v_cache  device uint8, kv4_cache_bytes(num_pages, ...) each.
+ * Per (token, head): y = fp32(fp64(exact(H+-1 . x)) * RN64(1/sqrt(D))); per
+ * 32-channel group e = clamp(floor(log2 max|y|) - 2, -127, 127) (e = -127 for
+ * an all-zero group); code = RNE_E2M1_saturating(y / 2^e) with the sign bit
+ * kept for values that round to zero; the scale byte is e + 127.
+ * Codes and scales are bit-exact for vectors whose exact Hadamard sum is
+ * representable in binary64 (in-vector dynamic range below about 2^40).
+ * Concurrent appends to the two tokens sharing a V byte are safe. */
+kv4_status kv4_append_quantize(const void* k, const void* v, int num_tokens, int num_kv_heads,
+                               int head_dim, const int32_t* slot_mapping, uint8_t* k_cache,
+                               uint8_t* v_cache, int num_pages, int page_size, int32_t* dev_error,
+                               kv4_stream_t stream);
+
+/* Number of KV splits the decode uses when called with num_splits = 0. */
+int kv4_decode_auto_splits(int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                           int head_dim, int page_size, int max_pages_per_seq);
+
+/* Workspace bytes for kv4_decode_attention / fp8_decode_attention with the
+ * given split count: partial outputs fp32 [B][T][Hq][S][D] and log-sum-exp
+ * fp32 [B][T][Hq][S]. */
+size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int head_dim,
+                                  int num_splits);
+
+/* Paged decode attention over the 4-bit cache ("What is UltraQuant", "Why
+ * UltraQuant beats 8-bit KV"; T > 1 is the MTP verify block of
+ * "Throughput-latency trade-off").
+ *   q             device bf16 [batch][q_per_seq][num_q_heads][head_dim], unrotated.
+ *                 Query head hq reads kv head hq / (num_q_heads/num_kv_heads).
+ *   k_cache       device, layout above.  v_cache: device, or NULL / == k_cache
+ *                 for the latent cache (K = V = latent row).
+ *   block_tables  device int32 [batch][max_pages_per_seq] physical page ids.
+ *   context_lens  device int32 [batch]: tokens in the cache for each sequence,
+ *                 counting the q_per_seq new ones.  Query position j attends
+ *                 to tokens t < context_lens[b] - q_per_seq + 1 + j.
+ *   softmax_scale multiplies q.k before the softmax.
+ *   num_splits    KV splits per sequence (0 = kv4_decode_auto_splits).
+ *   workspace     device, >= kv4_decode_workspace_bytes(...) bytes.
+ *   out           device fp32 [batch][q_per_seq][num_q_heads][head_dim],
+ *                 unrotated: out = softmax(s q.k) . v over the dequantised cache.
+ * Runs the split decode kernel then kv4_split_combine. */
+kv4_status kv4_decode_attention(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                                int head_dim, int page_size, int max_pages_per_seq, int num_pages,
+                                float softmax_scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, float* out, int32_t* dev_error,
+                                kv4_stream_t stream);
+
+/* The split stage of kv4_decode_attention alone: writes the per-split
+ * partial outputs (rotated space, each normalised by its own softmax sum)
+ * and log-sum-exps into `workspace` laid out as described for
+ * kv4_split_combine (partial_o at offset 0, partial_lse at offset
+ * round_up(B*T*Hq*S*D*4, 256)).  num_splits must be > 0 here (use
+ * kv4_decode_auto_splits to pick one).  kv4_decode_attention is this call
+ * followed by kv4_split_combine. */
+kv4_status kv4_decode_partials(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                               int head_dim, int page_size, int max_pages_per_seq, int num_pages,
+                               float softmax_scale, int num_splits, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_error, kv4_stream_t stream);
+
+/* Log-sum-exp merge of split partials, then the inverse rotation:
+ *   lse = log sum_s exp(lse_s);  O = sum_s exp(lse_s - lse) O_s;  out = H_D O.
+ *   partial_o    device fp32 [batch][q_per_seq][num_q_heads][num_splits][head_dim]
+ *                (each O_s already normalised by its own softmax sum)
+ *   partial_lse  device fp32 [batch][q_per_seq][num_q_heads][num_splits]
+ *                (natural log; -inf marks an empty split)
+ *   out          device fp32 [batch][q_per_seq][num_q_heads][head_dim].
+ * The page does not describe a split or its merge; this is the standard
+ * blockwise-softmax merge. */
+kv4_status kv4_split_combine(const float* partial_o, const float* partial_lse, int batch,
+                             int q_per_seq, int num_q_heads, int head_dim, int num_splits,
+                             float* out, kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * FP8 comparator: the 8-bit KV cache the page measures UltraQuant against
+ * ("UltraQuant vs 8-bit KV": standard FP8 cache on the AITER backends).
+ * E4M3 (OCP) with one fp32 scale per kv head, no rotation.
+ * Block per (page, kv head): K [P][D] token-major bytes, V [D][P]
+ * channel-major bytes; block bytes = P*D.
+ * --------------------------------------------------------------------- */
+size_t fp8_cache_bytes(int num_pages, int num_kv_heads, int page_size, int head_dim);
+
+/* code = E4M3_RNE_satfinite(fp32(x * inv_scale[h])).
+ *   k_inv_scale, v_inv_scale  device fp32 [num_kv_heads]. */
+kv4_status fp8_append_quantize(const void* k, const void* v, int num_tokens, int num_kv_heads,
+                               int head_dim, const int32_t* slot_mapping,
+                               const float* k_inv_scale, const float* v_inv_scale,
+                               uint8_t* k_cache, uint8_t* v_cache, int num_pages, int page_size,
+                               int32_t* dev_error, kv4_stream_t stream);
+
+/* As kv4_decode_attention over the FP8 cache; k_scale, v_scale: device fp32
+ * [num_kv_heads] (dequantised value = E4M3 value * scale). */
+kv4_status fp8_decode_attention(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, const int32_t* context_lens,
+                                int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                                int head_dim, int page_size, int max_pages_per_seq, int num_pages,
+                                float softmax_scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, float* out, int32_t* dev_error,
+                                kv4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV4_H_ */

@@ -318,28 +318,33 @@ int orc_append_quantize(const uint16_t* k, const uint16_t* v, int num_tokens,
                         int page_size) {
   if (!is_pow2_dim(D) || page_size <= 0 || (page_size & 1)) return ORC_BAD_ARG;
   const size_t bb = orc_block_bytes(page_size, D);
-  int status = ORC_OK;
-  for (int i = 0; i < num_tokens; ++i) {
-    int slot = slot_mapping[i];
-    if (slot < 0) continue;
-    int page = slot / page_size, off = slot % page_size;
-    if (page >= num_pages) return ORC_BAD_ARG;
-    for (int h = 0; h < Hkv; ++h) {
+  for (int i = 0; i < num_tokens; ++i)
+    if (slot_mapping[i] >= 0 && slot_mapping[i] / page_size >= num_pages) return ORC_BAD_ARG;
+  int bad = 0, inexact = 0;
+  (void)hadamard_cached(D);
+  /* Heads write disjoint blocks, so they may run in parallel; the tokens of
+   * one head run in order (two tokens share each V byte). */
+#pragma omp parallel for schedule(static) reduction(|:bad, inexact)
+  for (int h = 0; h < Hkv; ++h) {
+    for (int i = 0; i < num_tokens; ++i) {
+      int slot = slot_mapping[i];
+      if (slot < 0) continue;
+      int page = slot / page_size, off = slot % page_size;
       uint8_t codes[512];
       int expo[16];
       int st = orc_quantize_vector(k + ((size_t)i * Hkv + h) * D, D, codes, expo);
-      if (st == ORC_BAD_ARG) return st;
-      if (st == ORC_INEXACT) status = ORC_INEXACT;
+      if (st == ORC_BAD_ARG) { bad = 1; continue; }
+      if (st == ORC_INEXACT) inexact = 1;
       orc_pack_k_token(k_cache + ((size_t)page * Hkv + h) * bb, page_size, D, off, codes, expo);
       if (v) {
         st = orc_quantize_vector(v + ((size_t)i * Hkv + h) * D, D, codes, expo);
-        if (st == ORC_BAD_ARG) return st;
-        if (st == ORC_INEXACT) status = ORC_INEXACT;
+        if (st == ORC_BAD_ARG) { bad = 1; continue; }
+        if (st == ORC_INEXACT) inexact = 1;
         orc_pack_v_token(v_cache + ((size_t)page * Hkv + h) * bb, page_size, D, off, codes, expo);
       }
     }
   }
-  return status;
+  return bad ? ORC_BAD_ARG : (inexact ? ORC_INEXACT : ORC_OK);
 }
 
 /* ------------------------------------------------------------------ */

@@ -1,0 +1,88 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry
+point that include/kv4.h declares, and validates arguments on the host
+before launching anything (these calls return before touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_kv_cache_rotate_b300 as kv4
+from bit_kv_cache_rotate_b300 import build as kbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kv4.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", src, flags=re.M))
+                  - {"if", "extern"})
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kv4.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("kv4_append_quantize", "kv4_decode_attention", "kv4_split_combine",
+              "fp8_append_quantize", "fp8_decode_attention"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(kv4.EXPORTS) <= set(_declared())
+
+
+def test_sizes(lib):
+    assert kv4.kv4_cache_bytes(16384, 8, 16, 128) == 16384 * 8 * 1088
+    assert kv4.kv4_cache_bytes(1, 1, 16, 512) == 16 * 256 + 16 * 16
+    assert kv4.fp8_cache_bytes(10, 8, 16, 128) == 10 * 8 * 2048
+    assert kv4.kv4_cache_bytes(-1, 1, 16, 128) == 0
+    ws = kv4.kv4_decode_workspace_bytes(32, 1, 64, 128, 4)
+    assert ws >= 32 * 64 * 4 * (128 + 1) * 4
+    assert 1 <= kv4.kv4_decode_auto_splits(32, 1, 64, 8, 128, 16, 2048) <= 2048
+
+
+def test_host_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(4096)
+    # null pointers
+    assert lib.kv4_append_quantize(None, None, 4, 8, 128, None, None, None, 10, 16, None, None) == \
+        kv4.KV4_ERR_INVALID_ARG
+    # unsupported head dim / page size
+    assert lib.kv4_append_quantize(fake, fake, 4, 8, 96, fake, fake, fake, 10, 16, None, None) == \
+        kv4.KV4_ERR_UNSUPPORTED
+    assert lib.kv4_append_quantize(fake, fake, 4, 8, 128, fake, fake, fake, 10, 32, None, None) == \
+        kv4.KV4_ERR_UNSUPPORTED
+    # v without v_cache
+    assert lib.kv4_append_quantize(fake, fake, 4, 8, 128, fake, fake, None, 10, 16, None, None) == \
+        kv4.KV4_ERR_INVALID_ARG
+    # misaligned cache pointer
+    assert lib.kv4_append_quantize(fake, fake, 4, 8, 128, fake, P(4097), fake, 10, 16, None, None) == \
+        kv4.KV4_ERR_INVALID_ARG
+    # zero tokens is a no-op
+    assert lib.kv4_append_quantize(None, None, 0, 8, 128, None, None, None, 10, 16, None, None) == kv4.KV4_OK
+    # decode: Hq not a multiple of Hkv, T too large, workspace too small
+    dec = lib.kv4_decode_attention
+    args = lambda **kw: [kw.get("q", fake), fake, fake, fake, fake, kw.get("B", 2), kw.get("T", 1),
+                         kw.get("Hq", 8), kw.get("Hkv", 2), kw.get("D", 128), 16, 4, 8, 0.1,
+                         kw.get("S", 1), P(4096 * 256), kw.get("ws", 1 << 20), fake, None, None]
+    assert dec(*args(Hq=7)) == kv4.KV4_ERR_INVALID_ARG
+    assert dec(*args(T=9)) == kv4.KV4_ERR_UNSUPPORTED
+    assert dec(*args(D=80)) == kv4.KV4_ERR_UNSUPPORTED
+    assert dec(*args(ws=16)) == kv4.KV4_ERR_INVALID_ARG
+    assert dec(*args(q=None)) == kv4.KV4_ERR_INVALID_ARG
+    assert dec(*args(B=0)) == kv4.KV4_OK
+    assert lib.kv4_split_combine(None, None, 1, 1, 8, 128, 2, None, None) == kv4.KV4_ERR_INVALID_ARG
+    assert lib.kv4_split_combine(fake, fake, 1, 1, 8, 100, 2, fake, None) == kv4.KV4_ERR_UNSUPPORTED
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert lib.kv4_status_string(s)
