@@ -1,17 +1,615 @@
-// kv4_decode_mma.cu -- tensor-core decode path (filled in below).
+// kv4_decode_mma.cu -- tensor-core split decode over the 4-bit cache (sm_103a).
+//
+// "UltraQuant on AMD Instinct", section "What is UltraQuant": the codes stay
+// FP4 until the matrix units; the power-of-two scale is applied as part of
+// the multiply, no lookup table.  On B300 the warp-level tensor instructions
+// take e4m3 or f16 operands, so the codes are widened on the fly:
+//
+//   Q.K^T   e4m3 MMA (m16n8k32).  A K nibble (s|e1 e0|m) becomes an e4m3 byte
+//           by moving the sign to bit 7 and the magnitude to bits 4..2 -- the
+//           e4m3 value is then exactly code * 2^-6 (the 0.5 code lands on the
+//           e4m3 subnormal 2^-7).  Seven integer ops widen 8 codes.  q (rotated
+//           in fp32, scaled per row by a power of two) is split into four e4m3
+//           terms: rows g of each MMA carry terms 0 and 1, rows g+8 carry terms
+//           2 and 3 of the residual rescaled by 2^k, so the row's two
+//           accumulators combine as top + 2^-k bottom and resolve q to about
+//           2^-20 of its largest element.
+//           Each 32-channel group accumulates separately and is multiplied by
+//           its UE8M0 scale 2^e (a float built from the scale byte).
+//   P.V     f16 MMA (m16n8k16), swap-AB: O^T[dims x rows] += V^T P^T.  V codes
+//           are widened by the hardware E2M1->f16 conversion (exact) and
+//           multiplied by 2^(e_v - Eref_G), Eref_G being a running maximum of
+//           the group's V exponents (O rows of the group are rescaled when it
+//           grows).  P is split into f16 hi + lo parts (Veltkamp), so P.V
+//           carries about 22 bits of P.
+//
+// Work split: one CTA per (split, kv head, sequence); 4 consumer warps each
+// own every 4th chunk of 4 pages (64 tokens) of the split, with their own
+// online-softmax state, and merge at the end.  Each warp streams its chunks
+// with 1-D bulk copies (TMA, cp.async.bulk) into a private ring of shared-
+// memory stages completed through mbarriers.  Every wait is bounded: on
+// timeout the kernel flags KV4_DEVERR_TIMEOUT and stops.
 #include "kv4_common.cuh"
 #include "kv4_decode.h"
 
 namespace kv4 {
+namespace fast {
 
-bool fast_path_supported(int D, int G, int T, bool latent) {
-  (void)D; (void)G; (void)T; (void)latent;
+constexpr int D = 128;
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kPagesPerChunk = 4;
+constexpr int kBlk = kPage * D / 2 + kPage * D / 32;  // 1088 bytes per (page, head) block
+constexpr int kCodeBytes = kPage * D / 2;            // 1024
+constexpr int kBlkStride = 1104;                     // smem stride between staged blocks (bank spread)
+constexpr int kStageBytes = 2 * kPagesPerChunk * kBlkStride;  // K blocks then V blocks
+constexpr int kStages = 2;
+constexpr int kKTab = kPagesPerChunk * kPage * 4 * 4;  // fp32 [4 pages][16 tokens][4 groups]
+constexpr int kVTab = kPagesPerChunk * 8 * 4 * 4;      // f16x2 [4 pages][8 pairs][4 groups]
+constexpr int kWarpBytes = kStages * kStageBytes + kKTab + kVTab;
+constexpr int kQBytes = 8 * 4 * D;                     // e4m3 terms [8 rows][4 terms][128 ch]
+constexpr int kSmem = kWarps * kWarpBytes + kQBytes + 64;
+constexpr long long kSpinLimit = 1ll << 26;
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  for (long long i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
   return false;
 }
 
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One byte of two E2M1 codes -> f16x2 (low nibble -> low half), exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t word, int byte) {
+  uint32_t out;
+  const uint32_t b = word >> (8 * byte);
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(out) : "r"(b));
+  return out;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// 8 E2M1 codes (one 32-bit word, code i in bits 4i+3..4i) -> two words of
+// e4m3 bytes holding code * 2^-6: `lo` gets the even codes (bytes 0..3 =
+// codes 0,2,4,6), `hi` the odd codes.
+__device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  lo = ((x << 4) & 0x80808080u) | ((x << 2) & 0x1C1C1C1Cu);
+  hi = (x & 0x80808080u) | ((x >> 2) & 0x1C1C1C1Cu);
+}
+
+// Split x >= 0 into f16-exact hi (11 significant bits, Veltkamp) and the rest.
+// The _rn intrinsics keep the compiler from contracting the steps into an FMA,
+// which would compute x * 2^13 exactly and break the split.
+__device__ __forceinline__ void split_hi_lo(float x, float& hi, float& lo) {
+  const float c = __fmul_rn(x, 8193.0f);
+  hi = __fsub_rn(c, __fsub_rn(c, x));
+  lo = __fsub_rn(x, hi);
+}
+
+struct Smem {
+  uint8_t* base;
+  __device__ uint8_t* stage(int w, int s) const { return base + w * kWarpBytes + s * kStageBytes; }
+  __device__ float* ktab(int w) const {
+    return reinterpret_cast<float*>(base + w * kWarpBytes + kStages * kStageBytes);
+  }
+  __device__ uint32_t* vtab(int w) const {
+    return reinterpret_cast<uint32_t*>(base + w * kWarpBytes + kStages * kStageBytes + kKTab);
+  }
+  __device__ uint8_t* qterms() const { return base + kWarps * kWarpBytes; }
+  __device__ uint64_t* bars() const {
+    return reinterpret_cast<uint64_t*>(base + kWarps * kWarpBytes + kQBytes);
+  }
+};
+
+// ---------------------------------------------------------------- kernel
+// Rows: the R = T*G query rows of one kv head, R <= 8 (row r -> position
+// r / G, query head h*G + r % G); unused rows carry zero q and are never
+// written.
+__global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem sm{smem_raw};
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = a.Hq / a.Hkv;
+  const int R = a.T * G;
+  const int L = a.context_lens[b];
+  const size_t row0 = (size_t)b * a.T * a.Hq;
+
+  auto row_index = [&](int r) -> size_t {  // flat (b, j, hq) row of query row r
+    return row0 + (size_t)(r / G) * a.Hq + h * G + (r % G);
+  };
+  auto write_empty = [&]() {
+    for (int r = w; r < R; r += kWarps) {
+      const size_t rr = row_index(r) * a.S + s;
+      for (int d = lane; d < D; d += 32) a.part_o[rr * D + d] = 0.0f;
+      if (lane == 0) a.part_lse[rr] = -INFINITY;
+    }
+  };
+  if (L < a.T || L > a.max_pages * kPage) {
+    if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
+    write_empty();
+    return;
+  }
+  const int n_pages = (L + kPage - 1) / kPage;
+  const int per = (n_pages + a.S - 1) / a.S;
+  const int p0 = s * per;
+  const int p1 = min(n_pages, p0 + per);
+  if (p0 >= p1) {
+    write_empty();
+    return;
+  }
+  const int n_chunks = (p1 - p0 + kPagesPerChunk - 1) / kPagesPerChunk;
+  const int32_t* table = a.block_tables + (size_t)b * a.max_pages;
+  uint64_t* bars = sm.bars();  // [kWarps][kStages]
+
+  // ---- barriers
+  if (lane == 0)
+    for (int i = 0; i < kStages; ++i) mbar_init(&bars[w * kStages + i], 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+  // ---- issue helper: chunk c of this warp into stage st (lane 0 issues)
+  auto issue = [&](int c, int st) {
+    const int pg = p0 + c * kPagesPerChunk;
+    const int nv = min(kPagesPerChunk, p1 - pg);
+    int page = 0;
+    if (lane < nv) {
+      page = table[pg + lane];
+      if (page < 0 || page >= a.num_pages) {  // flagged; the page is read as page 0
+        flag_error(a.dev_error, KV4_DEVERR_PAGE);
+        page = 0;
+      }
+    }
+    uint8_t* dst = sm.stage(w, st);
+    uint64_t* bar = &bars[w * kStages + st];
+    if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nv * 2 * kBlk));
+    __syncwarp();
+    if (lane < nv) {
+      const size_t blk = ((size_t)page * a.Hkv + h) * kBlk;
+      bulk_g2s(dst + lane * kBlkStride, a.k_cache + blk, kBlk, bar);
+      bulk_g2s(dst + (kPagesPerChunk + lane) * kBlkStride, a.v_cache + blk, kBlk, bar);
+    }
+  };
+
+  // Start streaming before the q prologue so the first loads overlap it.
+  __syncthreads();
+  fence_proxy_async();
+  for (int i = 0; i < kStages; ++i) {
+    const int c = w + kWarps * i;
+    if (c < n_chunks) issue(c, i);
+  }
+
+  // ---- q prologue: rotate (fp32 butterfly), scale row by 2^sigma, 4 e4m3 terms
+  uint8_t* qt = sm.qterms();  // [8 rows][4 terms][128]
+  __shared__ float row_c[8];
+  __shared__ float row_c2[8];
+  __shared__ int row_limit[8];
+  for (int r = w; r < 8; r += kWarps) {
+    float x[4];
+    if (r < R) {
+      const uint16_t* src = a.q + row_index(r) * D + lane * 4;
+      const uint2 raw = *reinterpret_cast<const uint2*>(src);
+      x[0] = bf16_bits_to_float(raw.x & 0xFFFFu);
+      x[1] = bf16_bits_to_float(raw.x >> 16);
+      x[2] = bf16_bits_to_float(raw.y & 0xFFFFu);
+      x[3] = bf16_bits_to_float(raw.y >> 16);
+      fwht_warp<4, float>(x);
+    } else {
+      x[0] = x[1] = x[2] = x[3] = 0.0f;
+    }
+    float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // sigma puts the row maximum in [128, 256): x * 2^sigma is exact.
+    int sigma = 0;
+    if (mx > 0.0f) sigma = 7 - (int)((__float_as_uint(mx) >> 23) & 0xFF) + 127;
+    sigma = max(-120, min(120, sigma));
+    const float sc = __uint_as_float((uint32_t)(127 + sigma) << 23);
+    float rem[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rem[i] = x[i] * sc;
+    // Terms 0 and 1 at the row scale; the residual after them is rescaled by
+    // 2^k (its maximum brought to [128, 256)) and split into terms 2 and 3, so
+    // the four terms resolve q to about 2^-20 of its largest element.
+    int k2 = 0;
+#pragma unroll
+    for (int term = 0; term < 4; ++term) {
+      if (term == 2) {
+        float rm = fmaxf(fmaxf(fabsf(rem[0]), fabsf(rem[1])), fmaxf(fabsf(rem[2]), fabsf(rem[3])));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, o));
+        const int eb = (int)((__float_as_uint(rm) >> 23) & 0xFF);
+        k2 = eb == 0 ? 0 : max(0, min(120, 134 - eb));
+        const float up = __uint_as_float((uint32_t)(127 + k2) << 23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rem[i] *= up;
+      }
+      const uint32_t p01 = f32x2_to_e4m3x2(rem[0], rem[1]);
+      const uint32_t p23 = f32x2_to_e4m3x2(rem[2], rem[3]);
+      const float2 v01 = e4m3x2_to_f32x2(p01);
+      const float2 v23 = e4m3x2_to_f32x2(p23);
+      rem[0] -= v01.x;
+      rem[1] -= v01.y;
+      rem[2] -= v23.x;
+      rem[3] -= v23.y;
+      *reinterpret_cast<uint32_t*>(qt + (r * 4 + term) * D + lane * 4) = p01 | (p23 << 16);
+    }
+    if (lane == 0) {
+      // score = (sum of terms . code*2^-6 * 2^e) * 2^(6 - sigma) * softmax_scale*log2e/sqrt(D)
+      row_c[r] = a.qscale * __uint_as_float((uint32_t)(127 + 6 - sigma) << 23);
+      row_c2[r] = __uint_as_float((uint32_t)(127 - k2) << 23);  // weight of the bottom-row terms
+      row_limit[r] = r < R ? L - a.T + 1 + r / G : 0;
+    }
+  }
+  __syncthreads();
+
+  // A fragments: per group G, two MMAs: top rows = terms (0 | 1), bottom = terms (2 | 3).
+  uint32_t qa[4][2][4];
+#pragma unroll
+  for (int G4 = 0; G4 < 4; ++G4) {
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const uint2 top = *reinterpret_cast<const uint2*>(qt + (g * 4 + pr) * D + 32 * G4 + 8 * t);
+      const uint2 bot = *reinterpret_cast<const uint2*>(qt + (g * 4 + pr + 2) * D + 32 * G4 + 8 * t);
+      qa[G4][pr][0] = __byte_perm(top.x, top.y, 0x6420);  // row g, even channels
+      qa[G4][pr][1] = __byte_perm(bot.x, bot.y, 0x6420);  // row g+8
+      qa[G4][pr][2] = __byte_perm(top.x, top.y, 0x7531);  // row g, odd channels
+      qa[G4][pr][3] = __byte_perm(bot.x, bot.y, 0x7531);
+    }
+  }
+  const float my_c = row_c[g];
+  const float my_c2 = row_c2[g];
+  const int my_limit = row_limit[g];
+
+  // ---- per-warp running state
+  float o[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
+  float m_run = -INFINITY, l_part = 0.0f;
+  uint32_t eref = 0;  // 4 UE8M0 bytes: running max of V exponents per group
+
+  float* ktab = sm.ktab(w);
+  uint32_t* vtab = sm.vtab(w);
+  bool timed_out = false;
+  int it_fail = 0;
+
+  for (int c = w, it = 0; c < n_chunks; c += kWarps, ++it) {
+    const int st = it % kStages;
+    const uint32_t parity = (uint32_t)((it / kStages) & 1);
+    if (!mbar_wait(&bars[w * kStages + st], parity)) {
+      timed_out = true;
+      it_fail = it;
+      break;
+    }
+    const uint8_t* stg = sm.stage(w, st);
+    const int pg = p0 + c * kPagesPerChunk;
+    const int nv = min(kPagesPerChunk, p1 - pg);
+
+    // ---- scale tables: lane -> page lane>>3, tokens 2(lane&7), +1
+    {
+      const int pp = lane >> 3, tk = 2 * (lane & 7);
+      const int pos = (pg + pp) * kPage + tk;
+      uint32_t k0 = 0, k1 = 0, v0 = 0, v1 = 0;
+      if (pp < nv) {
+        const uint8_t* kb = stg + pp * kBlkStride + kCodeBytes;
+        const uint8_t* vb = stg + (kPagesPerChunk + pp) * kBlkStride + kCodeBytes;
+        if (pos < L) {
+          k0 = *reinterpret_cast<const uint32_t*>(kb + tk * 4);
+          v0 = *reinterpret_cast<const uint32_t*>(vb + tk * 4);
+        }
+        if (pos + 1 < L) {
+          k1 = *reinterpret_cast<const uint32_t*>(kb + tk * 4 + 4);
+          v1 = *reinterpret_cast<const uint32_t*>(vb + tk * 4 + 4);
+        }
+      }
+      uint32_t cm = __vmaxu4(v0, v1);
+#pragma unroll
+      for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
+      const uint32_t enew = __vmaxu4(eref, cm);
+      // rescale factors for O rows of each group: 2^(eref - enew)
+      float fg[4];
+      bool any = false;
+#pragma unroll
+      for (int G4 = 0; G4 < 4; ++G4) {
+        const int eo = (eref >> (8 * G4)) & 0xFF, en = (enew >> (8 * G4)) & 0xFF;
+        any |= eo != en;
+        const int ex = 127 + eo - en;
+        fg[G4] = ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f;
+      }
+      eref = enew;
+      // K scale floats 2^e (byte 0 -> 0.0: an all-zero-code group)
+      float4 f0, f1;
+      f0.x = __uint_as_float((k0 & 0xFFu) << 23);
+      f0.y = __uint_as_float(((k0 >> 8) & 0xFFu) << 23);
+      f0.z = __uint_as_float(((k0 >> 16) & 0xFFu) << 23);
+      f0.w = __uint_as_float((k0 >> 24) << 23);
+      f1.x = __uint_as_float((k1 & 0xFFu) << 23);
+      f1.y = __uint_as_float(((k1 >> 8) & 0xFFu) << 23);
+      f1.z = __uint_as_float(((k1 >> 16) & 0xFFu) << 23);
+      f1.w = __uint_as_float((k1 >> 24) << 23);
+      reinterpret_cast<float4*>(ktab)[(pp * kPage + tk) ] = f0;
+      reinterpret_cast<float4*>(ktab)[(pp * kPage + tk + 1)] = f1;
+      // V scale pairs 2^(e_v - Eref_G) as f16x2 (token tk low, tk+1 high)
+      uint4 vp;
+      uint32_t* vpp = reinterpret_cast<uint32_t*>(&vp);
+#pragma unroll
+      for (int G4 = 0; G4 < 4; ++G4) {
+        const int en = (enew >> (8 * G4)) & 0xFF;
+        uint32_t hv[2];
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int eb = (int)(((q2 ? v1 : v0) >> (8 * G4)) & 0xFF);
+          const int d = eb - en;  // <= 0
+          uint32_t bits = 0;
+          if (eb != 0) {
+            if (d >= -14) bits = (uint32_t)(d + 15) << 10;
+            else if (d >= -24) bits = 1u << (d + 24);
+          }
+          hv[q2] = bits;
+        }
+        vpp[G4] = hv[0] | (hv[1] << 16);
+      }
+      reinterpret_cast<uint4*>(vtab)[pp * 8 + (lane & 7)] = vp;
+      __syncwarp();
+
+      // ---- Q.K^T: 8 n8 tiles; tile n covers tokens 2n, 2n+1 of each page
+      float sc[16];
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        float acc[4][4];
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) acc[G4][0] = acc[G4][1] = acc[G4][2] = acc[G4][3] = 0.0f;
+        const uint8_t* krow = stg + (g >> 1) * kBlkStride + (2 * n + (g & 1)) * (D / 2) + 4 * t;
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) {
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(krow + 16 * G4);
+          uint32_t lo, hi;
+          e2m1x8_to_e4m3(x, lo, hi);
+          mma_e4m3(acc[G4], qa[G4][0], lo, hi);
+          mma_e4m3(acc[G4], qa[G4][1], lo, hi);
+        }
+        const float4 s0 = reinterpret_cast<const float4*>(ktab)[t * kPage + 2 * n];
+        const float4 s1 = reinterpret_cast<const float4*>(ktab)[t * kPage + 2 * n + 1];
+        float v0s = s0.x * fmaf(my_c2, acc[0][2], acc[0][0]);
+        v0s = fmaf(s0.y, fmaf(my_c2, acc[1][2], acc[1][0]), v0s);
+        v0s = fmaf(s0.z, fmaf(my_c2, acc[2][2], acc[2][0]), v0s);
+        v0s = fmaf(s0.w, fmaf(my_c2, acc[3][2], acc[3][0]), v0s);
+        float v1s = s1.x * fmaf(my_c2, acc[0][3], acc[0][1]);
+        v1s = fmaf(s1.y, fmaf(my_c2, acc[1][3], acc[1][1]), v1s);
+        v1s = fmaf(s1.z, fmaf(my_c2, acc[2][3], acc[2][1]), v1s);
+        v1s = fmaf(s1.w, fmaf(my_c2, acc[3][3], acc[3][1]), v1s);
+        const int posb = (pg + t) * kPage + 2 * n;
+        const bool ok = t < nv;
+        sc[2 * n] = (ok && posb < my_limit) ? v0s * my_c : -INFINITY;
+        sc[2 * n + 1] = (ok && posb + 1 < my_limit) ? v1s * my_c : -INFINITY;
+      }
+
+      // ---- online softmax for row g over this chunk (the quad t=0..3 holds the row)
+      float cmx = sc[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) cmx = fmaxf(cmx, sc[i]);
+      cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
+      cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
+      const float m_new = fmaxf(m_run, cmx);
+      float alpha = 1.0f;
+      float p[16];
+      if (m_new == -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p[i] = 0.0f;
+      } else {
+        alpha = exp2f(m_run - m_new);
+        float ls = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          p[i] = exp2f(sc[i] - m_new);
+          ls += p[i];
+        }
+        l_part = l_part * alpha + ls;
+      }
+      m_run = m_new;
+
+      // ---- rescale O: columns 2t, 2t+1 are query rows 2t, 2t+1
+      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+      if (__any_sync(0xffffffffu, any || a0 != 1.0f || a1 != 1.0f)) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float f = fg[j >> 1];
+          o[j][0] *= f * a0;
+          o[j][1] *= f * a1;
+          o[j][2] *= f * a0;
+          o[j][3] *= f * a1;
+        }
+      }
+
+      // ---- P fragments (hi + lo f16): k-step c4 uses tokens 4c4..4c4+3 of page t
+      uint32_t ph[4][2], pl[4][2];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float hi0, lo0, hi1, lo1, hi2, lo2, hi3, lo3;
+        split_hi_lo(p[4 * c4 + 0], hi0, lo0);
+        split_hi_lo(p[4 * c4 + 1], hi1, lo1);
+        split_hi_lo(p[4 * c4 + 2], hi2, lo2);
+        split_hi_lo(p[4 * c4 + 3], hi3, lo3);
+        ph[c4][0] = pack_f16x2(hi0, hi1);
+        ph[c4][1] = pack_f16x2(hi2, hi3);
+        pl[c4][0] = pack_f16x2(lo0, lo1);
+        pl[c4][1] = pack_f16x2(lo2, lo3);
+      }
+
+      // ---- P.V: m-tile j = dims 16j..16j+15 (group j/2); rows g, g+8 -> dims 16j+g, 16j+g+8
+      const uint8_t* vbase = stg + (kPagesPerChunk + t) * kBlkStride;
+#pragma unroll
+      for (int G4 = 0; G4 < 4; ++G4) {
+        uint32_t vsc[8];
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr) vsc[pr] = vtab[(t * 8 + pr) * 4 + G4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * G4 + jj;
+          const uint2 rA = *reinterpret_cast<const uint2*>(vbase + (16 * j + g) * (kPage / 2));
+          const uint2 rB = *reinterpret_cast<const uint2*>(vbase + (16 * j + g + 8) * (kPage / 2));
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            // bytes 2c4 (tokens 4c4, 4c4+1) and 2c4+1 (tokens 4c4+2, 4c4+3)
+            const uint32_t wA = c4 < 2 ? rA.x : rA.y;
+            const uint32_t wB = c4 < 2 ? rB.x : rB.y;
+            const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
+            const uint32_t x0 = hmul2(e2m1x2_to_f16x2(wA, b0), vsc[2 * c4]);
+            const uint32_t x1 = hmul2(e2m1x2_to_f16x2(wB, b0), vsc[2 * c4]);
+            const uint32_t x2 = hmul2(e2m1x2_to_f16x2(wA, b1), vsc[2 * c4 + 1]);
+            const uint32_t x3 = hmul2(e2m1x2_to_f16x2(wB, b1), vsc[2 * c4 + 1]);
+            mma_f16(o[j], x0, x1, x2, x3, ph[c4][0], ph[c4][1]);
+            mma_f16(o[j], x0, x1, x2, x3, pl[c4][0], pl[c4][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    // refill this stage with the warp's chunk kStages ahead
+    const int cn = c + kWarps * kStages;
+    if (cn < n_chunks) {
+      fence_proxy_async();
+      issue(cn, st);
+    }
+  }
+
+  if (timed_out) {
+    // Stop streaming, but let every copy this warp issued land before the
+    // shared memory is reused: iterations it_fail .. it_fail + kStages - 1 were
+    // issued and not yet waited on (each wait again bounded).
+    if (lane == 0) flag_error(a.dev_error, KV4_DEVERR_TIMEOUT);
+    for (int it = it_fail; it < it_fail + kStages; ++it)
+      if (w + kWarps * it < n_chunks)
+        (void)mbar_wait(&bars[w * kStages + it % kStages], (uint32_t)((it / kStages) & 1));
+  }
+
+  // ---- merge the 4 warps: row l sums, then O scaled by 2^Eref_G and exp2(m_w - M)
+  float l_row = l_part;
+  l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+  l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+  __syncthreads();  // all warps done with their stages: reuse smem for the merge
+  // Drain: make sure no bulk copy of this CTA is still landing (bounded).
+  float* mo = reinterpret_cast<float*>(smem_raw);  // [kWarps][8 rows][D]
+  float* mm = mo + kWarps * 8 * D;                  // [kWarps][8]
+  float* ml = mm + kWarps * 8;                      // [kWarps][8]
+  if (t == 0) {
+    mm[w * 8 + g] = m_run;
+    ml[w * 8 + g] = l_row;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float eg = __uint_as_float(((eref >> (8 * (j >> 1))) & 0xFFu) << 23);
+    mo[(w * 8 + 2 * t) * D + 16 * j + g] = o[j][0] * eg;
+    mo[(w * 8 + 2 * t + 1) * D + 16 * j + g] = o[j][1] * eg;
+    mo[(w * 8 + 2 * t) * D + 16 * j + g + 8] = o[j][2] * eg;
+    mo[(w * 8 + 2 * t + 1) * D + 16 * j + g + 8] = o[j][3] * eg;
+  }
+  __syncthreads();
+  // warp w finalises rows w and w+4
+  for (int r = w; r < 8; r += kWarps) {
+    if (r >= R) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mm[ww * 8 + r]);
+    float wsum = 0.0f, wt[kWarps];
+#pragma unroll
+    for (int ww = 0; ww < kWarps; ++ww) {
+      wt[ww] = (M == -INFINITY || mm[ww * 8 + r] == -INFINITY) ? 0.0f : exp2f(mm[ww * 8 + r] - M);
+      wsum += wt[ww] * ml[ww * 8 + r];
+    }
+    const size_t rr = row_index(r) * a.S + s;
+    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+    for (int d = lane; d < D; d += 32) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) acc = fmaf(wt[ww], mo[(ww * 8 + r) * D + d], acc);
+      a.part_o[rr * D + d] = acc * inv;
+    }
+    if (lane == 0) a.part_lse[rr] = wsum > 0.0f ? (M + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+}  // namespace fast
+
+bool fast_path_supported(int D, int G, int T, bool latent) {
+  return D == 128 && !latent && T * G <= 8;
+}
+
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
-  (void)D; (void)a; (void)st;
-  return cudaErrorNotSupported;
+  if (D != 128) return cudaErrorNotSupported;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(fast::decode_fp4_mma_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, fast::kSmem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const dim3 grid(a.S, a.Hkv, a.B);
+  fast::decode_fp4_mma_kernel<<<grid, fast::kThreads, fast::kSmem, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace kv4

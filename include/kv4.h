@@ -69,6 +69,7 @@ typedef enum {
 #define KV4_DEVERR_PAGE 1      /* block_tables entry outside [0, num_pages) */
 #define KV4_DEVERR_CONTEXT 2   /* context_lens[b] outside [q_per_seq, max_pages*page_size] */
 #define KV4_DEVERR_SLOT 4      /* slot_mapping entry outside the cache */
+#define KV4_DEVERR_TIMEOUT 8   /* a bounded wait for streamed cache data gave up */
 
 /* Human-readable name of a status. */
 const char* kv4_status_string(kv4_status s);
