@@ -7,7 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kv4.h"
+#include "kv4.h"
 
 namespace kv4 {
 

@@ -23,13 +23,15 @@ struct DecodeArgs {
   float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
 };
 
-// Splits per sequence: enough CTAs to fill every SM a few times over, never
-// more splits than pages.
+// Splits per sequence: about seven waves of two CTAs per SM (short waves keep
+// the tail small, more splits add partial-output traffic), at least four
+// pages per split.
 inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
   (void)head_dim;
-  const int target = 2 * sms;
-  int s = (target + units - 1) / units;
-  if (s > max_pages) s = max_pages;
+  const int target = 14 * sms;
+  int s = (target + units / 2) / units;
+  const int cap = max_pages / 4 > 0 ? max_pages / 4 : 1;
+  if (s > cap) s = cap;
   if (s > 256) s = 256;
   return s < 1 ? 1 : s;
 }

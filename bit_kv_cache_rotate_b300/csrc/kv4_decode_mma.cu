@@ -41,15 +41,21 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kPagesPerChunk = 4;
 constexpr int kBlk = kPage * D / 2 + kPage * D / 32;  // 1088 bytes per (page, head) block
 constexpr int kCodeBytes = kPage * D / 2;            // 1024
-constexpr int kBlkStride = 1104;                     // smem stride between staged blocks (bank spread)
-constexpr int kStageBytes = 2 * kPagesPerChunk * kBlkStride;  // K blocks then V blocks
-constexpr int kStages = 2;
-constexpr int kKTab = kPagesPerChunk * kPage * 4 * 4;  // fp32 [4 pages][16 tokens][4 groups]
-constexpr int kVTab = kPagesPerChunk * 8 * 4 * 4;      // f16x2 [4 pages][8 pairs][4 groups]
-constexpr int kWarpBytes = kStages * kStageBytes + kKTab + kVTab;
-constexpr int kQBytes = 8 * 4 * D;                     // e4m3 terms [8 rows][4 terms][128 ch]
-constexpr int kSmem = kWarps * kWarpBytes + kQBytes + 64;
-constexpr long long kSpinLimit = 1ll << 26;
+constexpr int kBlkStride = 1104;                     // smem stride between staged K blocks (bank spread)
+constexpr int kVStride = 1120;                       // smem stride between staged V blocks (bank spread)
+constexpr int kStageBytes = kPagesPerChunk * (kBlkStride + kVStride);  // K blocks then V blocks
+constexpr int kStages = 3;
+// Scale tables, rows padded so the four t-lanes of a quad hit distinct banks.
+constexpr int kKTabPage = 272;                     // fp32 [8 token pairs][4 groups][2 tokens] + pad
+constexpr int kVTabPage = 160;                     // f16x2 [4 groups][8 token pairs] + pad
+constexpr int kKTab = kPagesPerChunk * kKTabPage;
+constexpr int kVTab = kPagesPerChunk * kVTabPage;
+constexpr int kTabBytes = kKTab + kVTab;
+constexpr int kQBytes = 8 * 4 * D;                 // e4m3 terms [8 rows][4 terms][128 ch], aliases the tables
+static_assert(kWarps * kTabBytes >= kQBytes, "q terms must fit in the table area");
+constexpr int kSmem = kWarps * kStages * kStageBytes + kWarps * kTabBytes + 8 * kWarps * kStages;
+constexpr int kSpinLimit = 1 << 16;     // try_wait rounds, each suspending up to kSuspendNs
+constexpr uint32_t kSuspendNs = 20000;
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -65,17 +71,18 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// Bounded wait for the phase with the given parity; false on timeout.
+// Bounded wait for the phase with the given parity; false on timeout.  The
+// suspend hint lets a waiting warp sleep instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t addr = smem_u32(bar);
-  for (long long i = 0; i < kSpinLimit; ++i) {
+  for (int i = 0; i < kSpinLimit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(addr), "r"(parity)
+        : "r"(addr), "r"(parity), "r"(kSuspendNs)
         : "memory");
     if (done) return true;
   }
@@ -139,27 +146,32 @@ __device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t x, uint32_t& lo, uint32_
   hi = (x & 0x80808080u) | ((x >> 2) & 0x1C1C1C1Cu);
 }
 
-// Split x >= 0 into f16-exact hi (11 significant bits, Veltkamp) and the rest.
-// The _rn intrinsics keep the compiler from contracting the steps into an FMA,
-// which would compute x * 2^13 exactly and break the split.
-__device__ __forceinline__ void split_hi_lo(float x, float& hi, float& lo) {
-  const float c = __fmul_rn(x, 8193.0f);
-  hi = __fsub_rn(c, __fsub_rn(c, x));
-  lo = __fsub_rn(x, hi);
+// Split a pair x >= 0 into f16-exact hi parts (11 significant bits, Veltkamp)
+// and the remainders.  Packed fp32x2 ops with explicit rounding: no step can
+// be contracted into an FMA, which would break the split.
+__device__ __forceinline__ void split_hi_lo2(float2 x, float2& hi, float2& lo) {
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+  const float2 c = __fmul2_rn(x, make_float2(8193.0f, 8193.0f));
+  const float2 t = __ffma2_rn(x, m1, c);   // c - x
+  hi = __ffma2_rn(t, m1, c);               // c - (c - x)
+  lo = __ffma2_rn(hi, m1, x);              // x - hi (exact)
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 struct Smem {
   uint8_t* base;
-  __device__ uint8_t* stage(int w, int s) const { return base + w * kWarpBytes + s * kStageBytes; }
-  __device__ float* ktab(int w) const {
-    return reinterpret_cast<float*>(base + w * kWarpBytes + kStages * kStageBytes);
-  }
-  __device__ uint32_t* vtab(int w) const {
-    return reinterpret_cast<uint32_t*>(base + w * kWarpBytes + kStages * kStageBytes + kKTab);
-  }
-  __device__ uint8_t* qterms() const { return base + kWarps * kWarpBytes; }
+  __device__ uint8_t* stage(int w, int s) const { return base + (w * kStages + s) * kStageBytes; }
+  __device__ uint8_t* tabs(int w) const { return base + kWarps * kStages * kStageBytes + w * kTabBytes; }
+  __device__ float* ktab(int w) const { return reinterpret_cast<float*>(tabs(w)); }
+  __device__ uint32_t* vtab(int w) const { return reinterpret_cast<uint32_t*>(tabs(w) + kKTab); }
+  __device__ uint8_t* qterms() const { return tabs(0); }  // prologue only
   __device__ uint64_t* bars() const {
-    return reinterpret_cast<uint64_t*>(base + kWarps * kWarpBytes + kQBytes);
+    return reinterpret_cast<uint64_t*>(base + kWarps * kStages * kStageBytes + kWarps * kTabBytes);
   }
 };
 
@@ -210,18 +222,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     for (int i = 0; i < kStages; ++i) mbar_init(&bars[w * kStages + i], 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
-  // ---- issue helper: chunk c of this warp into stage st (lane 0 issues)
-  auto issue = [&](int c, int st) {
+  // Page ids of chunk c for lanes 0..3 (page 0 for lanes past the split; a
+  // bad id is flagged and read as page 0).
+  auto chunk_page = [&](int c) -> int {
     const int pg = p0 + c * kPagesPerChunk;
-    const int nv = min(kPagesPerChunk, p1 - pg);
     int page = 0;
-    if (lane < nv) {
+    if (lane < kPagesPerChunk && pg + lane < p1) {
       page = table[pg + lane];
-      if (page < 0 || page >= a.num_pages) {  // flagged; the page is read as page 0
+      if (page < 0 || page >= a.num_pages) {
         flag_error(a.dev_error, KV4_DEVERR_PAGE);
         page = 0;
       }
     }
+    return page;
+  };
+  // Issue chunk c into stage st: lane i < nv copies page i's K and V blocks.
+  auto issue = [&](int c, int st, int page) {
+    const int nv = min(kPagesPerChunk, p1 - (p0 + c * kPagesPerChunk));
     uint8_t* dst = sm.stage(w, st);
     uint64_t* bar = &bars[w * kStages + st];
     if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nv * 2 * kBlk));
@@ -229,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     if (lane < nv) {
       const size_t blk = ((size_t)page * a.Hkv + h) * kBlk;
       bulk_g2s(dst + lane * kBlkStride, a.k_cache + blk, kBlk, bar);
-      bulk_g2s(dst + (kPagesPerChunk + lane) * kBlkStride, a.v_cache + blk, kBlk, bar);
+      bulk_g2s(dst + kPagesPerChunk * kBlkStride + lane * kVStride, a.v_cache + blk, kBlk, bar);
     }
   };
 
@@ -238,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
   fence_proxy_async();
   for (int i = 0; i < kStages; ++i) {
     const int c = w + kWarps * i;
-    if (c < n_chunks) issue(c, i);
+    if (c < n_chunks) issue(c, i, chunk_page(c));
   }
 
   // ---- q prologue: rotate (fp32 butterfly), scale row by 2^sigma, 4 e4m3 terms
@@ -264,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     // sigma puts the row maximum in [128, 256): x * 2^sigma is exact.
     int sigma = 0;
-    if (mx > 0.0f) sigma = 7 - (int)((__float_as_uint(mx) >> 23) & 0xFF) + 127;
+    if (mx > 0.0f) sigma = 134 - (int)((__float_as_uint(mx) >> 23) & 0xFF);
     sigma = max(-120, min(120, sigma));
     const float sc = __uint_as_float((uint32_t)(127 + sigma) << 23);
     float rem[4];
@@ -297,10 +314,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
       *reinterpret_cast<uint32_t*>(qt + (r * 4 + term) * D + lane * 4) = p01 | (p23 << 16);
     }
     if (lane == 0) {
-      // score = (sum of terms . code*2^-6 * 2^e) * 2^(6 - sigma) * softmax_scale*log2e/sqrt(D)
+      // score*log2e = (terms . code*2^-6 * 2^e) * 2^(6 - sigma) * softmax_scale*log2e/sqrt(D)
       row_c[r] = a.qscale * __uint_as_float((uint32_t)(127 + 6 - sigma) << 23);
       row_c2[r] = __uint_as_float((uint32_t)(127 - k2) << 23);  // weight of the bottom-row terms
-      row_limit[r] = r < R ? L - a.T + 1 + r / G : 0;
+      row_limit[r] = r < R ? L - a.T + 1 + r / G : 0x7fffffff;
     }
   }
   __syncthreads();
@@ -320,14 +337,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     }
   }
   const float my_c = row_c[g];
-  const float my_c2 = row_c2[g];
+  const float2 my_c2 = make_float2(row_c2[g], row_c2[g]);
   const int my_limit = row_limit[g];
+  int min_limit = row_limit[0];
+#pragma unroll
+  for (int r = 1; r < 8; ++r) min_limit = min(min_limit, row_limit[r]);
+  __syncthreads();  // the q terms share memory with the scale tables
 
   // ---- per-warp running state
   float o[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
-  float m_run = -INFINITY, l_part = 0.0f;
+  float m_run = -INFINITY;
+  float2 l2 = make_float2(0.0f, 0.0f);
   uint32_t eref = 0;  // 4 UE8M0 bytes: running max of V exponents per group
 
   float* ktab = sm.ktab(w);
@@ -338,6 +360,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
   for (int c = w, it = 0; c < n_chunks; c += kWarps, ++it) {
     const int st = it % kStages;
     const uint32_t parity = (uint32_t)((it / kStages) & 1);
+    // page ids for the refill of this stage, loaded now to hide their latency
+    const int cn = c + kWarps * kStages;
+    const int next_page = cn < n_chunks ? chunk_page(cn) : 0;
     if (!mbar_wait(&bars[w * kStages + st], parity)) {
       timed_out = true;
       it_fail = it;
@@ -346,57 +371,51 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     const uint8_t* stg = sm.stage(w, st);
     const int pg = p0 + c * kPagesPerChunk;
     const int nv = min(kPagesPerChunk, p1 - pg);
+    const bool edge = nv < kPagesPerChunk || (pg + kPagesPerChunk) * kPage > min_limit;
 
-    // ---- scale tables: lane -> page lane>>3, tokens 2(lane&7), +1
+    // ---- scale tables: lane -> page lane>>3, token pair lane&7
+    float fg[4];
+    bool any_e;
     {
-      const int pp = lane >> 3, tk = 2 * (lane & 7);
+      const int pp = lane >> 3, pr = lane & 7, tk = 2 * pr;
       const int pos = (pg + pp) * kPage + tk;
       uint32_t k0 = 0, k1 = 0, v0 = 0, v1 = 0;
       if (pp < nv) {
         const uint8_t* kb = stg + pp * kBlkStride + kCodeBytes;
-        const uint8_t* vb = stg + (kPagesPerChunk + pp) * kBlkStride + kCodeBytes;
-        if (pos < L) {
-          k0 = *reinterpret_cast<const uint32_t*>(kb + tk * 4);
-          v0 = *reinterpret_cast<const uint32_t*>(vb + tk * 4);
-        }
-        if (pos + 1 < L) {
-          k1 = *reinterpret_cast<const uint32_t*>(kb + tk * 4 + 4);
-          v1 = *reinterpret_cast<const uint32_t*>(vb + tk * 4 + 4);
-        }
+        const uint8_t* vb = stg + kPagesPerChunk * kBlkStride + pp * kVStride + kCodeBytes;
+        const uint2 kk = *reinterpret_cast<const uint2*>(kb + tk * 4);
+        const uint2 vv = *reinterpret_cast<const uint2*>(vb + tk * 4);
+        if (pos < L) { k0 = kk.x; v0 = vv.x; }
+        if (pos + 1 < L) { k1 = kk.y; v1 = vv.y; }
       }
       uint32_t cm = __vmaxu4(v0, v1);
 #pragma unroll
       for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
       const uint32_t enew = __vmaxu4(eref, cm);
-      // rescale factors for O rows of each group: 2^(eref - enew)
-      float fg[4];
-      bool any = false;
+      any_e = enew != eref;
 #pragma unroll
       for (int G4 = 0; G4 < 4; ++G4) {
-        const int eo = (eref >> (8 * G4)) & 0xFF, en = (enew >> (8 * G4)) & 0xFF;
-        any |= eo != en;
-        const int ex = 127 + eo - en;
+        const int ex = 127 + (int)((eref >> (8 * G4)) & 0xFF) - (int)((enew >> (8 * G4)) & 0xFF);
         fg[G4] = ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f;
       }
       eref = enew;
-      // K scale floats 2^e (byte 0 -> 0.0: an all-zero-code group)
-      float4 f0, f1;
-      f0.x = __uint_as_float((k0 & 0xFFu) << 23);
-      f0.y = __uint_as_float(((k0 >> 8) & 0xFFu) << 23);
-      f0.z = __uint_as_float(((k0 >> 16) & 0xFFu) << 23);
-      f0.w = __uint_as_float((k0 >> 24) << 23);
-      f1.x = __uint_as_float((k1 & 0xFFu) << 23);
-      f1.y = __uint_as_float(((k1 >> 8) & 0xFFu) << 23);
-      f1.z = __uint_as_float(((k1 >> 16) & 0xFFu) << 23);
-      f1.w = __uint_as_float((k1 >> 24) << 23);
-      reinterpret_cast<float4*>(ktab)[(pp * kPage + tk) ] = f0;
-      reinterpret_cast<float4*>(ktab)[(pp * kPage + tk + 1)] = f1;
-      // V scale pairs 2^(e_v - Eref_G) as f16x2 (token tk low, tk+1 high)
-      uint4 vp;
-      uint32_t* vpp = reinterpret_cast<uint32_t*>(&vp);
+      // K scale pairs: {2^e(tk,G), 2^e(tk+1,G)} for G = 0..3 (byte 0 -> 0.0)
+      float4 f01, f23;
+      f01.x = __uint_as_float((k0 & 0xFFu) << 23);
+      f01.y = __uint_as_float((k1 & 0xFFu) << 23);
+      f01.z = __uint_as_float((k0 >> 8 & 0xFFu) << 23);
+      f01.w = __uint_as_float((k1 >> 8 & 0xFFu) << 23);
+      f23.x = __uint_as_float((k0 >> 16 & 0xFFu) << 23);
+      f23.y = __uint_as_float((k1 >> 16 & 0xFFu) << 23);
+      f23.z = __uint_as_float((k0 >> 24) << 23);
+      f23.w = __uint_as_float((k1 >> 24) << 23);
+      float4* kt = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(ktab) + pp * kKTabPage + pr * 32);
+      kt[0] = f01;
+      kt[1] = f23;
+      // V scale pairs 2^(e_v - Eref_G) as f16x2 (token tk low half, tk+1 high half)
 #pragma unroll
       for (int G4 = 0; G4 < 4; ++G4) {
-        const int en = (enew >> (8 * G4)) & 0xFF;
+        const int en = (int)((enew >> (8 * G4)) & 0xFF);
         uint32_t hv[2];
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
@@ -409,130 +428,153 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
           }
           hv[q2] = bits;
         }
-        vpp[G4] = hv[0] | (hv[1] << 16);
+        vtab[pp * (kVTabPage / 4) + G4 * 8 + pr] = hv[0] | (hv[1] << 16);
       }
-      reinterpret_cast<uint4*>(vtab)[pp * 8 + (lane & 7)] = vp;
       __syncwarp();
+    }
 
-      // ---- Q.K^T: 8 n8 tiles; tile n covers tokens 2n, 2n+1 of each page
-      float sc[16];
+    // ---- Q.K^T: 8 n8 tiles, two at a time (8 independent accumulator chains);
+    // tile n covers token pair n of each page (col 2t'+i -> page t', token 2n+i)
+    float2 sc[8];  // row g, tokens (2n, 2n+1) of page t
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
-        float acc[4][4];
+    for (int n = 0; n < 8; n += 2) {
+      float acc[2][4][4];
 #pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4) acc[G4][0] = acc[G4][1] = acc[G4][2] = acc[G4][3] = 0.0f;
-        const uint8_t* krow = stg + (g >> 1) * kBlkStride + (2 * n + (g & 1)) * (D / 2) + 4 * t;
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) acc[u][G4][0] = acc[u][G4][1] = acc[u][G4][2] = acc[u][G4][3] = 0.0f;
+      uint32_t klo[2][4], khi[2][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint8_t* krow = stg + (g >> 1) * kBlkStride + (2 * (n + u) + (g & 1)) * (D / 2) + 4 * t;
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
           const uint32_t x = *reinterpret_cast<const uint32_t*>(krow + 16 * G4);
-          uint32_t lo, hi;
-          e2m1x8_to_e4m3(x, lo, hi);
-          mma_e4m3(acc[G4], qa[G4][0], lo, hi);
-          mma_e4m3(acc[G4], qa[G4][1], lo, hi);
-        }
-        const float4 s0 = reinterpret_cast<const float4*>(ktab)[t * kPage + 2 * n];
-        const float4 s1 = reinterpret_cast<const float4*>(ktab)[t * kPage + 2 * n + 1];
-        float v0s = s0.x * fmaf(my_c2, acc[0][2], acc[0][0]);
-        v0s = fmaf(s0.y, fmaf(my_c2, acc[1][2], acc[1][0]), v0s);
-        v0s = fmaf(s0.z, fmaf(my_c2, acc[2][2], acc[2][0]), v0s);
-        v0s = fmaf(s0.w, fmaf(my_c2, acc[3][2], acc[3][0]), v0s);
-        float v1s = s1.x * fmaf(my_c2, acc[0][3], acc[0][1]);
-        v1s = fmaf(s1.y, fmaf(my_c2, acc[1][3], acc[1][1]), v1s);
-        v1s = fmaf(s1.z, fmaf(my_c2, acc[2][3], acc[2][1]), v1s);
-        v1s = fmaf(s1.w, fmaf(my_c2, acc[3][3], acc[3][1]), v1s);
-        const int posb = (pg + t) * kPage + 2 * n;
-        const bool ok = t < nv;
-        sc[2 * n] = (ok && posb < my_limit) ? v0s * my_c : -INFINITY;
-        sc[2 * n + 1] = (ok && posb + 1 < my_limit) ? v1s * my_c : -INFINITY;
-      }
-
-      // ---- online softmax for row g over this chunk (the quad t=0..3 holds the row)
-      float cmx = sc[0];
-#pragma unroll
-      for (int i = 1; i < 16; ++i) cmx = fmaxf(cmx, sc[i]);
-      cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
-      cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
-      const float m_new = fmaxf(m_run, cmx);
-      float alpha = 1.0f;
-      float p[16];
-      if (m_new == -INFINITY) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) p[i] = 0.0f;
-      } else {
-        alpha = exp2f(m_run - m_new);
-        float ls = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          p[i] = exp2f(sc[i] - m_new);
-          ls += p[i];
-        }
-        l_part = l_part * alpha + ls;
-      }
-      m_run = m_new;
-
-      // ---- rescale O: columns 2t, 2t+1 are query rows 2t, 2t+1
-      const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
-      const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-      if (__any_sync(0xffffffffu, any || a0 != 1.0f || a1 != 1.0f)) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float f = fg[j >> 1];
-          o[j][0] *= f * a0;
-          o[j][1] *= f * a1;
-          o[j][2] *= f * a0;
-          o[j][3] *= f * a1;
+          e2m1x8_to_e4m3(x, klo[u][G4], khi[u][G4]);
         }
       }
-
-      // ---- P fragments (hi + lo f16): k-step c4 uses tokens 4c4..4c4+3 of page t
-      uint32_t ph[4][2], pl[4][2];
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float hi0, lo0, hi1, lo1, hi2, lo2, hi3, lo3;
-        split_hi_lo(p[4 * c4 + 0], hi0, lo0);
-        split_hi_lo(p[4 * c4 + 1], hi1, lo1);
-        split_hi_lo(p[4 * c4 + 2], hi2, lo2);
-        split_hi_lo(p[4 * c4 + 3], hi3, lo3);
-        ph[c4][0] = pack_f16x2(hi0, hi1);
-        ph[c4][1] = pack_f16x2(hi2, hi3);
-        pl[c4][0] = pack_f16x2(lo0, lo1);
-        pl[c4][1] = pack_f16x2(lo2, lo3);
-      }
-
-      // ---- P.V: m-tile j = dims 16j..16j+15 (group j/2); rows g, g+8 -> dims 16j+g, 16j+g+8
-      const uint8_t* vbase = stg + (kPagesPerChunk + t) * kBlkStride;
+      for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
-      for (int G4 = 0; G4 < 4; ++G4) {
-        uint32_t vsc[8];
+        for (int G4 = 0; G4 < 4; ++G4)
 #pragma unroll
-        for (int pr = 0; pr < 8; ++pr) vsc[pr] = vtab[(t * 8 + pr) * 4 + G4];
+          for (int u = 0; u < 2; ++u) mma_e4m3(acc[u][G4], qa[G4][pr], klo[u][G4], khi[u][G4]);
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * G4 + jj;
-          const uint2 rA = *reinterpret_cast<const uint2*>(vbase + (16 * j + g) * (kPage / 2));
-          const uint2 rB = *reinterpret_cast<const uint2*>(vbase + (16 * j + g + 8) * (kPage / 2));
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            // bytes 2c4 (tokens 4c4, 4c4+1) and 2c4+1 (tokens 4c4+2, 4c4+3)
-            const uint32_t wA = c4 < 2 ? rA.x : rA.y;
-            const uint32_t wB = c4 < 2 ? rB.x : rB.y;
-            const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
-            const uint32_t x0 = hmul2(e2m1x2_to_f16x2(wA, b0), vsc[2 * c4]);
-            const uint32_t x1 = hmul2(e2m1x2_to_f16x2(wB, b0), vsc[2 * c4]);
-            const uint32_t x2 = hmul2(e2m1x2_to_f16x2(wA, b1), vsc[2 * c4 + 1]);
-            const uint32_t x3 = hmul2(e2m1x2_to_f16x2(wB, b1), vsc[2 * c4 + 1]);
-            mma_f16(o[j], x0, x1, x2, x3, ph[c4][0], ph[c4][1]);
-            mma_f16(o[j], x0, x1, x2, x3, pl[c4][0], pl[c4][1]);
-          }
+      for (int u = 0; u < 2; ++u) {
+        const float4* kt =
+            reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(ktab) + t * kKTabPage + (n + u) * 32);
+        const float4 s01 = kt[0], s23 = kt[1];
+        float (&ac)[4][4] = acc[u];
+        float2 v = __fmul2_rn(make_float2(s01.x, s01.y),
+                              __ffma2_rn(my_c2, make_float2(ac[0][2], ac[0][3]), make_float2(ac[0][0], ac[0][1])));
+        v = __ffma2_rn(make_float2(s01.z, s01.w),
+                       __ffma2_rn(my_c2, make_float2(ac[1][2], ac[1][3]), make_float2(ac[1][0], ac[1][1])), v);
+        v = __ffma2_rn(make_float2(s23.x, s23.y),
+                       __ffma2_rn(my_c2, make_float2(ac[2][2], ac[2][3]), make_float2(ac[2][0], ac[2][1])), v);
+        v = __ffma2_rn(make_float2(s23.z, s23.w),
+                       __ffma2_rn(my_c2, make_float2(ac[3][2], ac[3][3]), make_float2(ac[3][0], ac[3][1])), v);
+        v = __fmul2_rn(v, make_float2(my_c, my_c));
+        if (edge) {
+          const int posb = (pg + t) * kPage + 2 * (n + u);
+          const bool ok = t < nv;
+          if (!(ok && posb < my_limit)) v.x = -INFINITY;
+          if (!(ok && posb + 1 < my_limit)) v.y = -INFINITY;
         }
+        sc[n + u] = v;
       }
+    }
+
+    // ---- online softmax for row g over this chunk (the quad t = 0..3 holds the row)
+    float cmx = fmaxf(sc[0].x, sc[0].y);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) cmx = fmaxf(cmx, fmaxf(sc[i].x, sc[i].y));
+    cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
+    cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
+    const float m_new = fmaxf(m_run, cmx);
+    float alpha = 1.0f;
+    float2 p[8];
+    if (m_new == -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = make_float2(0.0f, 0.0f);
+    } else {
+      alpha = ex2(m_run - m_new);
+      const float2 nm = make_float2(-m_new, -m_new);
+      float2 ls = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 d2 = __fadd2_rn(sc[i], nm);
+        p[i] = make_float2(ex2(d2.x), ex2(d2.y));
+        ls = __fadd2_rn(ls, p[i]);
+      }
+      l2 = __ffma2_rn(l2, make_float2(alpha, alpha), ls);
+    }
+    m_run = m_new;
+
+    // ---- rescale O: columns 2t, 2t+1 are query rows 2t, 2t+1
+    const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
+    const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+    if (__any_sync(0xffffffffu, any_e || a0 != 1.0f || a1 != 1.0f)) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float f = fg[j >> 1];
+        o[j][0] *= f * a0;
+        o[j][1] *= f * a1;
+        o[j][2] *= f * a0;
+        o[j][3] *= f * a1;
+      }
+    }
+
+    // ---- P fragments (hi + lo f16): k-step c4 uses tokens 4c4..4c4+3 of page t
+    uint32_t ph[4][2], pl[4][2];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      float2 h0, l0, h1, l1;
+      split_hi_lo2(p[2 * c4], h0, l0);
+      split_hi_lo2(p[2 * c4 + 1], h1, l1);
+      ph[c4][0] = pack_f16x2(h0.x, h0.y);
+      ph[c4][1] = pack_f16x2(h1.x, h1.y);
+      pl[c4][0] = pack_f16x2(l0.x, l0.y);
+      pl[c4][1] = pack_f16x2(l1.x, l1.y);
+    }
+
+    // ---- P.V: m-tile j = dims 16j..16j+15 (group j/2); rows g, g+8 -> dims 16j+g, 16j+g+8.
+    // Per k-step the hi MMAs of all 8 m-tiles issue before the lo MMAs, so no
+    // accumulator is updated twice in a row.
+    const uint8_t* vbase = stg + kPagesPerChunk * kBlkStride + t * kVStride;
+    uint2 rA[8], rB[8];
+#pragma unroll
+    for (int jt = 0; jt < 8; ++jt) {
+      rA[jt] = *reinterpret_cast<const uint2*>(vbase + (16 * jt + g) * (kPage / 2));
+      rB[jt] = *reinterpret_cast<const uint2*>(vbase + (16 * jt + g + 8) * (kPage / 2));
+    }
+    const uint32_t* vrow = vtab + t * (kVTabPage / 4);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      // bytes 2c4 (tokens 4c4, 4c4+1) and 2c4+1 (tokens 4c4+2, 4c4+3)
+      const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
+      uint2 vs[4];
+#pragma unroll
+      for (int G4 = 0; G4 < 4; ++G4) vs[G4] = *reinterpret_cast<const uint2*>(vrow + G4 * 8 + 2 * c4);
+      uint32_t xa[8][4];
+#pragma unroll
+      for (int jt = 0; jt < 8; ++jt) {
+        const uint32_t wA = c4 < 2 ? rA[jt].x : rA[jt].y, wB = c4 < 2 ? rB[jt].x : rB[jt].y;
+        const uint2 sv = vs[jt >> 1];
+        xa[jt][0] = hmul2(e2m1x2_to_f16x2(wA, b0), sv.x);
+        xa[jt][1] = hmul2(e2m1x2_to_f16x2(wB, b0), sv.x);
+        xa[jt][2] = hmul2(e2m1x2_to_f16x2(wA, b1), sv.y);
+        xa[jt][3] = hmul2(e2m1x2_to_f16x2(wB, b1), sv.y);
+        mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], ph[c4][0], ph[c4][1]);
+      }
+#pragma unroll
+      for (int jt = 0; jt < 8; ++jt)
+        mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], pl[c4][0], pl[c4][1]);
     }
     __syncwarp();
     // refill this stage with the warp's chunk kStages ahead
-    const int cn = c + kWarps * kStages;
     if (cn < n_chunks) {
       fence_proxy_async();
-      issue(cn, st);
+      issue(cn, st, next_page);
     }
   }
 
@@ -547,11 +589,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
   }
 
   // ---- merge the 4 warps: row l sums, then O scaled by 2^Eref_G and exp2(m_w - M)
-  float l_row = l_part;
+  float l_row = l2.x + l2.y;
   l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
   l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
   __syncthreads();  // all warps done with their stages: reuse smem for the merge
-  // Drain: make sure no bulk copy of this CTA is still landing (bounded).
   float* mo = reinterpret_cast<float*>(smem_raw);  // [kWarps][8 rows][D]
   float* mm = mo + kWarps * 8 * D;                  // [kWarps][8]
   float* ml = mm + kWarps * 8;                      // [kWarps][8]
