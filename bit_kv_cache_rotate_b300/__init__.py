@@ -216,6 +216,28 @@ def kv4_split_combine(partial_o: torch.Tensor, partial_lse: torch.Tensor,
     return out
 
 
+def kv4_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, num_kv_heads: int,
+                                 num_pages: int, softmax_scale: float, num_splits: int = 0,
+                                 out: torch.Tensor | None = None, dev_error=None,
+                                 page_size: int = PAGE_SIZE, stream=None) -> torch.Tensor:
+    """kv4_decode_attention without a workspace: for callers that cannot allocate
+    device memory.  The split partials go to a fixed array inside libkv4 shared
+    by all calls, so calls whose GPU work overlaps must be ordered."""
+    _dev(q, "q", torch.bfloat16)
+    B, T, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, T, Hq, D), dtype=torch.float32, device=q.device)
+    fn = lib().kv4_decode_attention_noalloc
+    P, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, P, P]
+    fn.restype = i32
+    st = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, T, Hq,
+            num_kv_heads, D, page_size, block_tables.shape[1], num_pages, float(softmax_scale), num_splits,
+            _ptr(out), _ptr(dev_error), _stream(stream))
+    _check("kv4_decode_attention_noalloc", st)
+    return out
+
+
 # ---------------------------------------------------------------- FP8 comparator
 def fp8_append_quantize(k, v, slot_mapping, k_inv_scale, v_inv_scale, k_cache, v_cache, num_pages,
                         page_size: int = PAGE_SIZE, dev_error=None, stream=None) -> None:

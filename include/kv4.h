@@ -148,6 +148,38 @@ kv4_status kv4_decode_partials(const void* q, const uint8_t* k_cache, const uint
                                float softmax_scale, int num_splits, void* workspace,
                                size_t workspace_bytes, int32_t* dev_error, kv4_stream_t stream);
 
+/* Decode attention for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point; it exists for callers
+ * such as operator plugins that the host framework hands only input and
+ * output buffers, or step loops that must not call cudaMalloc (it
+ * synchronises the device and can fail once a memory pool owns the GPU).
+ * Arguments and results are those of kv4_decode_attention without the
+ * workspace: the split partials live in a fixed array of
+ * KV4_NOALLOC_SCRATCH_BYTES bytes in device global memory that libkv4
+ * declares itself (every GPU that loads the library keeps it until exit).
+ * The call allocates nothing and calls no allocating routine.
+ *   - num_splits = 0 picks kv4_decode_auto_splits, lowered if needed to the
+ *     largest count whose partials (kv4_decode_workspace_bytes) fit.  An
+ *     explicit num_splits whose partials do not fit, or a request that does
+ *     not fit even with one split per sequence, returns KV4_ERR_INVALID_ARG
+ *     before anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls share the array, which keeps what the last call wrote.
+ *     Nothing in it has to start at zero: the kernels write every partial
+ *     they read back.  Calls whose GPU work overlaps (other streams, other
+ *     host threads without ordering) race on the array and give wrong
+ *     results; order them. */
+#define KV4_NOALLOC_SCRATCH_BYTES (16u << 20)
+kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
+                                        const uint8_t* v_cache, const int32_t* block_tables,
+                                        const int32_t* context_lens, int batch, int q_per_seq,
+                                        int num_q_heads, int num_kv_heads, int head_dim,
+                                        int page_size, int max_pages_per_seq, int num_pages,
+                                        float softmax_scale, int num_splits, float* out,
+                                        int32_t* dev_error, kv4_stream_t stream);
+
 /* Log-sum-exp merge of split partials, then the inverse rotation:
  *   lse = log sum_s exp(lse_s);  O = sum_s exp(lse_s - lse) O_s;  out = H_D O.
  *   partial_o    device fp32 [batch][q_per_seq][num_q_heads][num_splits][head_dim]
