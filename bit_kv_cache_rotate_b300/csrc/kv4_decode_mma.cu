@@ -374,8 +374,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     const bool edge = nv < kPagesPerChunk || (pg + kPagesPerChunk) * kPage > min_limit;
 
     // ---- scale tables: lane -> page lane>>3, token pair lane&7
-    float fg[4];
-    bool any_e;
+    uint32_t eold;
     {
       const int pp = lane >> 3, pr = lane & 7, tk = 2 * pr;
       const int pos = (pg + pp) * kPage + tk;
@@ -388,48 +387,49 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
         if (pos < L) { k0 = kk.x; v0 = vv.x; }
         if (pos + 1 < L) { k1 = kk.y; v1 = vv.y; }
       }
-      uint32_t cm = __vmaxu4(v0, v1);
+      // V reference exponent per group (Eref): fixed from the warp's first
+      // chunk, so the usual chunk needs no reduction.  The f16 scale factors
+      // 2^(e_v - Eref) hold exponents from -24 to +15; a chunk with an exponent
+      // more than 15 above Eref (a rare jump) raises Eref to the chunk maximum
+      // and the accumulators are rescaled below.
+      eold = eref;
+      const uint32_t lim = __vaddus4(eref, 0x0F0F0F0Fu);
+      const bool over = (__vcmpgtu4(v0, lim) | __vcmpgtu4(v1, lim)) != 0u;
+      if (it == 0 || __any_sync(0xffffffffu, over)) {
+        uint32_t cm = __vmaxu4(v0, v1);
 #pragma unroll
-      for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
-      const uint32_t enew = __vmaxu4(eref, cm);
-      any_e = enew != eref;
-#pragma unroll
-      for (int G4 = 0; G4 < 4; ++G4) {
-        const int ex = 127 + (int)((eref >> (8 * G4)) & 0xFF) - (int)((enew >> (8 * G4)) & 0xFF);
-        fg[G4] = ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f;
+        for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
+        eref = __vmaxu4(eref, cm);
       }
-      eref = enew;
       // K scale pairs: {2^e(tk,G), 2^e(tk+1,G)} for G = 0..3 (byte 0 -> 0.0)
       float4 f01, f23;
-      f01.x = __uint_as_float((k0 & 0xFFu) << 23);
-      f01.y = __uint_as_float((k1 & 0xFFu) << 23);
-      f01.z = __uint_as_float((k0 >> 8 & 0xFFu) << 23);
-      f01.w = __uint_as_float((k1 >> 8 & 0xFFu) << 23);
-      f23.x = __uint_as_float((k0 >> 16 & 0xFFu) << 23);
-      f23.y = __uint_as_float((k1 >> 16 & 0xFFu) << 23);
-      f23.z = __uint_as_float((k0 >> 24) << 23);
-      f23.w = __uint_as_float((k1 >> 24) << 23);
+      f01.x = __uint_as_float((k0 << 23) & 0x7F800000u);
+      f01.y = __uint_as_float((k1 << 23) & 0x7F800000u);
+      f01.z = __uint_as_float((k0 << 15) & 0x7F800000u);
+      f01.w = __uint_as_float((k1 << 15) & 0x7F800000u);
+      f23.x = __uint_as_float((k0 << 7) & 0x7F800000u);
+      f23.y = __uint_as_float((k1 << 7) & 0x7F800000u);
+      f23.z = __uint_as_float((k0 >> 1) & 0x7F800000u);
+      f23.w = __uint_as_float((k1 >> 1) & 0x7F800000u);
       float4* kt = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(ktab) + pp * kKTabPage + pr * 32);
       kt[0] = f01;
       kt[1] = f23;
-      // V scale pairs 2^(e_v - Eref_G) as f16x2 (token tk low half, tk+1 high half)
-#pragma unroll
-      for (int G4 = 0; G4 < 4; ++G4) {
-        const int en = (int)((enew >> (8 * G4)) & 0xFF);
-        uint32_t hv[2];
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          const int eb = (int)(((q2 ? v1 : v0) >> (8 * G4)) & 0xFF);
-          const int d = eb - en;  // <= 0
-          uint32_t bits = 0;
-          if (eb != 0) {
-            if (d >= -14) bits = (uint32_t)(d + 15) << 10;
-            else if (d >= -24) bits = 1u << (d + 24);
-          }
-          hv[q2] = bits;
-        }
-        vtab[pp * (kVTabPage / 4) + G4 * 8 + pr] = hv[0] | (hv[1] << 16);
-      }
+      // V scale pairs 2^(e_v - Eref_G) as f16x2 (token tk low half, tk+1 high half):
+      // f16 exponent field 15 + e_v - Eref per byte, in [0, 30] here; values
+      // below 2^-14 of the reference flush to zero.  A zero scale byte belongs
+      // to an all-zero-code group, whose values are zero whatever the scale.
+      const uint32_t a0 = __vsubus4(__vaddus4(v0, 0x0F0F0F0Fu), eref);
+      const uint32_t a1 = __vsubus4(__vaddus4(v1, 0x0F0F0F0Fu), eref);
+      uint4 vp;
+      vp.x = __byte_perm(__byte_perm(a0, a1, 0x0040), 0, 0x5140) << 10;
+      vp.y = __byte_perm(__byte_perm(a0, a1, 0x0051), 0, 0x5140) << 10;
+      vp.z = __byte_perm(__byte_perm(a0, a1, 0x0062), 0, 0x5140) << 10;
+      vp.w = __byte_perm(__byte_perm(a0, a1, 0x0073), 0, 0x5140) << 10;
+      uint32_t* vt = vtab + pp * (kVTabPage / 4) + pr;
+      vt[0] = vp.x;
+      vt[8] = vp.y;
+      vt[16] = vp.z;
+      vt[24] = vp.w;
       __syncwarp();
     }
 
@@ -465,15 +465,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
             reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(ktab) + t * kKTabPage + (n + u) * 32);
         const float4 s01 = kt[0], s23 = kt[1];
         float (&ac)[4][4] = acc[u];
-        float2 v = __fmul2_rn(make_float2(s01.x, s01.y),
-                              __ffma2_rn(my_c2, make_float2(ac[0][2], ac[0][3]), make_float2(ac[0][0], ac[0][1])));
-        v = __ffma2_rn(make_float2(s01.z, s01.w),
-                       __ffma2_rn(my_c2, make_float2(ac[1][2], ac[1][3]), make_float2(ac[1][0], ac[1][1])), v);
-        v = __ffma2_rn(make_float2(s23.x, s23.y),
-                       __ffma2_rn(my_c2, make_float2(ac[2][2], ac[2][3]), make_float2(ac[2][0], ac[2][1])), v);
-        v = __ffma2_rn(make_float2(s23.z, s23.w),
-                       __ffma2_rn(my_c2, make_float2(ac[3][2], ac[3][3]), make_float2(ac[3][0], ac[3][1])), v);
-        v = __fmul2_rn(v, make_float2(my_c, my_c));
+        const float2 t0 = __ffma2_rn(my_c2, make_float2(ac[0][2], ac[0][3]), make_float2(ac[0][0], ac[0][1]));
+        const float2 t1 = __ffma2_rn(my_c2, make_float2(ac[1][2], ac[1][3]), make_float2(ac[1][0], ac[1][1]));
+        const float2 t2 = __ffma2_rn(my_c2, make_float2(ac[2][2], ac[2][3]), make_float2(ac[2][0], ac[2][1]));
+        const float2 t3 = __ffma2_rn(my_c2, make_float2(ac[3][2], ac[3][3]), make_float2(ac[3][0], ac[3][1]));
+        const float2 v01 = __ffma2_rn(make_float2(s01.z, s01.w), t1, __fmul2_rn(make_float2(s01.x, s01.y), t0));
+        const float2 v23 = __ffma2_rn(make_float2(s23.z, s23.w), t3, __fmul2_rn(make_float2(s23.x, s23.y), t2));
+        float2 v = __fmul2_rn(__fadd2_rn(v01, v23), make_float2(my_c, my_c));
         if (edge) {
           const int posb = (pg + t) * kPage + 2 * (n + u);
           const bool ok = t < nv;
@@ -485,9 +483,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     }
 
     // ---- online softmax for row g over this chunk (the quad t = 0..3 holds the row)
-    float cmx = fmaxf(sc[0].x, sc[0].y);
+    float mx8[8];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) cmx = fmaxf(cmx, fmaxf(sc[i].x, sc[i].y));
+    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(sc[i].x, sc[i].y);
+#pragma unroll
+    for (int w2 = 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+      for (int i = 0; i < w2; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w2]);
+    float cmx = mx8[0];
     cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
     cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
     const float m_new = fmaxf(m_run, cmx);
@@ -499,33 +502,43 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     } else {
       alpha = ex2(m_run - m_new);
       const float2 nm = make_float2(-m_new, -m_new);
-      float2 ls = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float2 d2 = __fadd2_rn(sc[i], nm);
         p[i] = make_float2(ex2(d2.x), ex2(d2.y));
-        ls = __fadd2_rn(ls, p[i]);
       }
+      const float2 ls = __fadd2_rn(__fadd2_rn(__fadd2_rn(p[0], p[1]), __fadd2_rn(p[2], p[3])),
+                                   __fadd2_rn(__fadd2_rn(p[4], p[5]), __fadd2_rn(p[6], p[7])));
       l2 = __ffma2_rn(l2, make_float2(alpha, alpha), ls);
     }
     m_run = m_new;
 
-    // ---- rescale O: columns 2t, 2t+1 are query rows 2t, 2t+1
+    // ---- rescale O: columns 2t, 2t+1 are query rows 2t, 2t+1; group factor 2^(Eold - Enew)
     const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
     const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-    if (__any_sync(0xffffffffu, any_e || a0 != 1.0f || a1 != 1.0f)) {
+    if (__any_sync(0xffffffffu, eold != eref || a0 != 1.0f || a1 != 1.0f)) {
+      const uint32_t dl = __vsubus4(eref, eold);  // Enew - Eold per group
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float f = fg[j >> 1];
-        o[j][0] *= f * a0;
-        o[j][1] *= f * a1;
-        o[j][2] *= f * a0;
-        o[j][3] *= f * a1;
+      for (int G4 = 0; G4 < 4; ++G4) {
+        const int ex = 127 - (int)((dl >> (8 * G4)) & 0xFFu);
+        const float f = ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f;
+        const float f0 = f * a0, f1 = f * a1;
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          o[2 * G4 + jj][0] *= f0;
+          o[2 * G4 + jj][1] *= f1;
+          o[2 * G4 + jj][2] *= f0;
+          o[2 * G4 + jj][3] *= f1;
+        }
       }
     }
 
-    // ---- P fragments (hi + lo f16): k-step c4 uses tokens 4c4..4c4+3 of page t
+    // ---- P fragments (hi + lo f16): k-step c4 uses tokens 4c4..4c4+3 of page t.
+    // The lo part matters only for large p: its MMAs run for a k-step only when
+    // some p of the step (any row, any page) exceeds 2^-8; below that the f16
+    // rounding of p alone stays under 2^-20 per token.
     uint32_t ph[4][2], pl[4][2];
+    bool need_lo[4];
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
       float2 h0, l0, h1, l1;
@@ -535,11 +548,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
       ph[c4][1] = pack_f16x2(h1.x, h1.y);
       pl[c4][0] = pack_f16x2(l0.x, l0.y);
       pl[c4][1] = pack_f16x2(l1.x, l1.y);
+      const float pm = fmaxf(fmaxf(p[2 * c4].x, p[2 * c4].y), fmaxf(p[2 * c4 + 1].x, p[2 * c4 + 1].y));
+      need_lo[c4] = __any_sync(0xffffffffu, pm > 0.00390625f);
     }
 
     // ---- P.V: m-tile j = dims 16j..16j+15 (group j/2); rows g, g+8 -> dims 16j+g, 16j+g+8.
-    // Per k-step the hi MMAs of all 8 m-tiles issue before the lo MMAs, so no
-    // accumulator is updated twice in a row.
+    // V codes widen exactly to f16; the V scale 2^(e_v - Eref_G) multiplies the
+    // P fragments of group G instead (two tokens per f16x2, as in the A fragment).
     const uint8_t* vbase = stg + kPagesPerChunk * kBlkStride + t * kVStride;
     uint2 rA[8], rB[8];
 #pragma unroll
@@ -552,23 +567,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     for (int c4 = 0; c4 < 4; ++c4) {
       // bytes 2c4 (tokens 4c4, 4c4+1) and 2c4+1 (tokens 4c4+2, 4c4+3)
       const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
-      uint2 vs[4];
+      uint32_t xa[8][4], pgh[4][2], pgl[4][2];
 #pragma unroll
-      for (int G4 = 0; G4 < 4; ++G4) vs[G4] = *reinterpret_cast<const uint2*>(vrow + G4 * 8 + 2 * c4);
-      uint32_t xa[8][4];
+      for (int G4 = 0; G4 < 4; ++G4) {
+        const uint2 vs = *reinterpret_cast<const uint2*>(vrow + G4 * 8 + 2 * c4);
+        pgh[G4][0] = hmul2(ph[c4][0], vs.x);
+        pgh[G4][1] = hmul2(ph[c4][1], vs.y);
+        pgl[G4][0] = hmul2(pl[c4][0], vs.x);
+        pgl[G4][1] = hmul2(pl[c4][1], vs.y);
+      }
 #pragma unroll
       for (int jt = 0; jt < 8; ++jt) {
         const uint32_t wA = c4 < 2 ? rA[jt].x : rA[jt].y, wB = c4 < 2 ? rB[jt].x : rB[jt].y;
-        const uint2 sv = vs[jt >> 1];
-        xa[jt][0] = hmul2(e2m1x2_to_f16x2(wA, b0), sv.x);
-        xa[jt][1] = hmul2(e2m1x2_to_f16x2(wB, b0), sv.x);
-        xa[jt][2] = hmul2(e2m1x2_to_f16x2(wA, b1), sv.y);
-        xa[jt][3] = hmul2(e2m1x2_to_f16x2(wB, b1), sv.y);
-        mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], ph[c4][0], ph[c4][1]);
+        xa[jt][0] = e2m1x2_to_f16x2(wA, b0);
+        xa[jt][1] = e2m1x2_to_f16x2(wB, b0);
+        xa[jt][2] = e2m1x2_to_f16x2(wA, b1);
+        xa[jt][3] = e2m1x2_to_f16x2(wB, b1);
+        mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], pgh[jt >> 1][0], pgh[jt >> 1][1]);
       }
+      if (need_lo[c4]) {
 #pragma unroll
-      for (int jt = 0; jt < 8; ++jt)
-        mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], pl[c4][0], pl[c4][1]);
+        for (int jt = 0; jt < 8; ++jt)
+          mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], pgl[jt >> 1][0], pgl[jt >> 1][1]);
+      }
     }
     __syncwarp();
     // refill this stage with the warp's chunk kStages ahead
