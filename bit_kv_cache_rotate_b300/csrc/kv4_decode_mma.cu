@@ -3,32 +3,35 @@
 // "UltraQuant on AMD Instinct", section "What is UltraQuant": the codes stay
 // FP4 until the matrix units; the power-of-two scale is applied as part of
 // the multiply, no lookup table.  On B300 the warp-level tensor instructions
-// take e4m3 or f16 operands, so the codes are widened on the fly:
+// take f16 (or e4m3, measured at two f16 MMAs plus operand conversions and
+// adds each), so the codes are widened to f16 on the fly by the hardware
+// E2M1->f16 conversion, which is exact:
 //
-//   Q.K^T   e4m3 MMA (m16n8k32).  A K nibble (s|e1 e0|m) becomes an e4m3 byte
-//           by moving the sign to bit 7 and the magnitude to bits 4..2 -- the
-//           e4m3 value is then exactly code * 2^-6 (the 0.5 code lands on the
-//           e4m3 subnormal 2^-7).  Seven integer ops widen 8 codes.  q (rotated
-//           in fp32, scaled per row by a power of two) is split into four e4m3
-//           terms: rows g of each MMA carry terms 0 and 1, rows g+8 carry terms
-//           2 and 3 of the residual rescaled by 2^k, so the row's two
-//           accumulators combine as top + 2^-k bottom and resolve q to about
-//           2^-20 of its largest element.
+//   Q.K^T   f16 MMA (m16n8k16).  A K byte (two codes) becomes an f16x2 pair
+//           of the code values in one conversion.  q (rotated in fp32,
+//           scaled per row by a power of two) is split into an f16 hi part
+//           (MMA row g) and the f16-rounded remainder (row g+8), so the two
+//           rows' sum resolves q to about 2^-22 of its largest element.
 //           Each 32-channel group accumulates separately and is multiplied by
 //           its UE8M0 scale 2^e (a float built from the scale byte).
 //   P.V     f16 MMA (m16n8k16), swap-AB: O^T[dims x rows] += V^T P^T.  V codes
-//           are widened by the hardware E2M1->f16 conversion (exact) and
-//           multiplied by 2^(e_v - Eref_G), Eref_G being a running maximum of
-//           the group's V exponents (O rows of the group are rescaled when it
-//           grows).  P is split into f16 hi + lo parts (Veltkamp), so P.V
+//           are widened the same way; the V scale enters as 2^(e_v - Eref_G)
+//           multiplied into the P fragments of group G, Eref_G being a per-
+//           warp reference exponent (O rows of the group are rescaled when it
+//           rises).  P is split into f16 hi + lo parts (Veltkamp), so P.V
 //           carries about 22 bits of P.
 //
 // Work split: one CTA per (split, kv head, sequence); 4 consumer warps each
 // own every 4th chunk of 4 pages (64 tokens) of the split, with their own
 // online-softmax state, and merge at the end.  Each warp streams its chunks
-// with 1-D bulk copies (TMA, cp.async.bulk) into a private ring of shared-
-// memory stages completed through mbarriers.  Every wait is bounded: on
-// timeout the kernel flags KV4_DEVERR_TIMEOUT and stops.
+// with 1-D bulk copies (TMA, cp.async.bulk) into private shared-memory stages
+// completed through mbarriers, refilling a stage as soon as it is consumed.
+// Three CTAs share an SM (registers capped at 168 per thread), so twelve
+// warps' copies and math overlap; one stage per warp measured faster than
+// two stages at two CTAs per SM.  Every wait is bounded: on timeout the
+// kernel flags KV4_DEVERR_TIMEOUT and stops.
+#include <cuda_fp16.h>
+
 #include "kv4_common.cuh"
 #include "kv4_decode.h"
 
@@ -44,14 +47,14 @@ constexpr int kCodeBytes = kPage * D / 2;            // 1024
 constexpr int kBlkStride = 1104;                     // smem stride between staged K blocks (bank spread)
 constexpr int kVStride = 1120;                       // smem stride between staged V blocks (bank spread)
 constexpr int kStageBytes = kPagesPerChunk * (kBlkStride + kVStride);  // K blocks then V blocks
-constexpr int kStages = 3;
+constexpr int kStages = 1;
 // Scale tables, rows padded so the four t-lanes of a quad hit distinct banks.
 constexpr int kKTabPage = 272;                     // fp32 [8 token pairs][4 groups][2 tokens] + pad
 constexpr int kVTabPage = 160;                     // f16x2 [4 groups][8 token pairs] + pad
 constexpr int kKTab = kPagesPerChunk * kKTabPage;
 constexpr int kVTab = kPagesPerChunk * kVTabPage;
 constexpr int kTabBytes = kKTab + kVTab;
-constexpr int kQBytes = 8 * 4 * D;                 // e4m3 terms [8 rows][4 terms][128 ch], aliases the tables
+constexpr int kQBytes = 8 * 2 * D * 2;             // f16 q [8 rows][hi, lo][128 ch], aliases the tables
 static_assert(kWarps * kTabBytes >= kQBytes, "q terms must fit in the table area");
 constexpr int kSmem = kWarps * kStages * kStageBytes + kWarps * kTabBytes + 8 * kWarps * kStages;
 constexpr int kSpinLimit = 1 << 16;     // try_wait rounds, each suspending up to kSuspendNs
@@ -101,14 +104,6 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -136,14 +131,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
-}
-
-// 8 E2M1 codes (one 32-bit word, code i in bits 4i+3..4i) -> two words of
-// e4m3 bytes holding code * 2^-6: `lo` gets the even codes (bytes 0..3 =
-// codes 0,2,4,6), `hi` the odd codes.
-__device__ __forceinline__ void e2m1x8_to_e4m3(uint32_t x, uint32_t& lo, uint32_t& hi) {
-  lo = ((x << 4) & 0x80808080u) | ((x << 2) & 0x1C1C1C1Cu);
-  hi = (x & 0x80808080u) | ((x >> 2) & 0x1C1C1C1Cu);
 }
 
 // Split a pair x >= 0 into f16-exact hi parts (11 significant bits, Veltkamp)
@@ -179,7 +166,7 @@ struct Smem {
 // Rows: the R = T*G query rows of one kv head, R <= 8 (row r -> position
 // r / G, query head h*G + r % G); unused rows carry zero q and are never
 // written.
-__global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) decode_fp4_mma_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem sm{smem_raw};
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -258,10 +245,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     if (c < n_chunks) issue(c, i, chunk_page(c));
   }
 
-  // ---- q prologue: rotate (fp32 butterfly), scale row by 2^sigma, 4 e4m3 terms
-  uint8_t* qt = sm.qterms();  // [8 rows][4 terms][128]
+  // ---- q prologue: rotate (fp32 butterfly), scale row by 2^sigma, split into f16 hi + lo
+  uint16_t* qt = reinterpret_cast<uint16_t*>(sm.qterms());  // [8 rows][hi, lo][128]
   __shared__ float row_c[8];
-  __shared__ float row_c2[8];
   __shared__ int row_limit[8];
   for (int r = w; r < 8; r += kWarps) {
     float x[4];
@@ -279,65 +265,43 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    // sigma puts the row maximum in [128, 256): x * 2^sigma is exact.
+    // sigma puts the row maximum in [2^14, 2^15) (f16 range, lo parts far
+    // above the f16 subnormal floor); x * 2^sigma is exact.
     int sigma = 0;
-    if (mx > 0.0f) sigma = 134 - (int)((__float_as_uint(mx) >> 23) & 0xFF);
-    sigma = max(-120, min(120, sigma));
+    if (mx > 0.0f) sigma = max(-113, min(126, 141 - (int)((__float_as_uint(mx) >> 23) & 0xFF)));
     const float sc = __uint_as_float((uint32_t)(127 + sigma) << 23);
-    float rem[4];
+    uint32_t hw[2], lw[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) rem[i] = x[i] * sc;
-    // Terms 0 and 1 at the row scale; the residual after them is rescaled by
-    // 2^k (its maximum brought to [128, 256)) and split into terms 2 and 3, so
-    // the four terms resolve q to about 2^-20 of its largest element.
-    int k2 = 0;
-#pragma unroll
-    for (int term = 0; term < 4; ++term) {
-      if (term == 2) {
-        float rm = fmaxf(fmaxf(fabsf(rem[0]), fabsf(rem[1])), fmaxf(fabsf(rem[2]), fabsf(rem[3])));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, o));
-        const int eb = (int)((__float_as_uint(rm) >> 23) & 0xFF);
-        k2 = eb == 0 ? 0 : max(0, min(120, 134 - eb));
-        const float up = __uint_as_float((uint32_t)(127 + k2) << 23);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rem[i] *= up;
-      }
-      const uint32_t p01 = f32x2_to_e4m3x2(rem[0], rem[1]);
-      const uint32_t p23 = f32x2_to_e4m3x2(rem[2], rem[3]);
-      const float2 v01 = e4m3x2_to_f32x2(p01);
-      const float2 v23 = e4m3x2_to_f32x2(p23);
-      rem[0] -= v01.x;
-      rem[1] -= v01.y;
-      rem[2] -= v23.x;
-      rem[3] -= v23.y;
-      *reinterpret_cast<uint32_t*>(qt + (r * 4 + term) * D + lane * 4) = p01 | (p23 << 16);
+    for (int i = 0; i < 2; ++i) {
+      const float v0 = x[2 * i] * sc, v1 = x[2 * i + 1] * sc;
+      const uint32_t h = pack_f16x2(v0, v1);
+      const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      hw[i] = h;
+      lw[i] = pack_f16x2(v0 - hf.x, v1 - hf.y);  // exact remainders, rounded to f16
     }
+    *reinterpret_cast<uint2*>(qt + (r * 2) * D + lane * 4) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(qt + (r * 2 + 1) * D + lane * 4) = make_uint2(lw[0], lw[1]);
     if (lane == 0) {
-      // score*log2e = (terms . code*2^-6 * 2^e) * 2^(6 - sigma) * softmax_scale*log2e/sqrt(D)
-      row_c[r] = a.qscale * __uint_as_float((uint32_t)(127 + 6 - sigma) << 23);
-      row_c2[r] = __uint_as_float((uint32_t)(127 - k2) << 23);  // weight of the bottom-row terms
+      // score*log2e = (q*2^sigma . code * 2^e) * 2^-sigma * softmax_scale*log2e/sqrt(D)
+      row_c[r] = a.qscale * __uint_as_float((uint32_t)(127 - sigma) << 23);
       row_limit[r] = r < R ? L - a.T + 1 + r / G : 0x7fffffff;
     }
   }
   __syncthreads();
 
-  // A fragments: per group G, two MMAs: top rows = terms (0 | 1), bottom = terms (2 | 3).
+  // A fragments, per 32-channel group two k16 steps.  Row g holds hi, row g+8
+  // lo.  Step j's k index 2t+i maps to channel 32G + 8t + 4j + i and 2t+8+i to
+  // 32G + 8t + 4j + 2 + i, matching the K B-fragments built from one 32-bit
+  // word of codes per thread (bytes 4t .. 4t+3 of the group).
   uint32_t qa[4][2][4];
 #pragma unroll
   for (int G4 = 0; G4 < 4; ++G4) {
-#pragma unroll
-    for (int pr = 0; pr < 2; ++pr) {
-      const uint2 top = *reinterpret_cast<const uint2*>(qt + (g * 4 + pr) * D + 32 * G4 + 8 * t);
-      const uint2 bot = *reinterpret_cast<const uint2*>(qt + (g * 4 + pr + 2) * D + 32 * G4 + 8 * t);
-      qa[G4][pr][0] = __byte_perm(top.x, top.y, 0x6420);  // row g, even channels
-      qa[G4][pr][1] = __byte_perm(bot.x, bot.y, 0x6420);  // row g+8
-      qa[G4][pr][2] = __byte_perm(top.x, top.y, 0x7531);  // row g, odd channels
-      qa[G4][pr][3] = __byte_perm(bot.x, bot.y, 0x7531);
-    }
+    const uint4 hi = *reinterpret_cast<const uint4*>(qt + (g * 2) * D + 32 * G4 + 8 * t);
+    const uint4 lo = *reinterpret_cast<const uint4*>(qt + (g * 2 + 1) * D + 32 * G4 + 8 * t);
+    qa[G4][0][0] = hi.x; qa[G4][0][1] = lo.x; qa[G4][0][2] = hi.y; qa[G4][0][3] = lo.y;
+    qa[G4][1][0] = hi.z; qa[G4][1][1] = lo.z; qa[G4][1][2] = hi.w; qa[G4][1][3] = lo.w;
   }
   const float my_c = row_c[g];
-  const float2 my_c2 = make_float2(row_c2[g], row_c2[g]);
   const int my_limit = row_limit[g];
   int min_limit = row_limit[0];
 #pragma unroll
@@ -443,32 +407,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
       for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) acc[u][G4][0] = acc[u][G4][1] = acc[u][G4][2] = acc[u][G4][3] = 0.0f;
-      uint32_t klo[2][4], khi[2][4];
+      uint32_t kb[2][4][4];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const uint8_t* krow = stg + (g >> 1) * kBlkStride + (2 * (n + u) + (g & 1)) * (D / 2) + 4 * t;
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
           const uint32_t x = *reinterpret_cast<const uint32_t*>(krow + 16 * G4);
-          e2m1x8_to_e4m3(x, klo[u][G4], khi[u][G4]);
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) kb[u][G4][bb] = e2m1x2_to_f16x2(x, bb);
         }
       }
 #pragma unroll
-      for (int pr = 0; pr < 2; ++pr)
+      for (int j2 = 0; j2 < 2; ++j2)
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4)
 #pragma unroll
-          for (int u = 0; u < 2; ++u) mma_e4m3(acc[u][G4], qa[G4][pr], klo[u][G4], khi[u][G4]);
+          for (int u = 0; u < 2; ++u)
+            mma_f16(acc[u][G4], qa[G4][j2][0], qa[G4][j2][1], qa[G4][j2][2], qa[G4][j2][3],
+                    kb[u][G4][2 * j2], kb[u][G4][2 * j2 + 1]);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const float4* kt =
             reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(ktab) + t * kKTabPage + (n + u) * 32);
         const float4 s01 = kt[0], s23 = kt[1];
         float (&ac)[4][4] = acc[u];
-        const float2 t0 = __ffma2_rn(my_c2, make_float2(ac[0][2], ac[0][3]), make_float2(ac[0][0], ac[0][1]));
-        const float2 t1 = __ffma2_rn(my_c2, make_float2(ac[1][2], ac[1][3]), make_float2(ac[1][0], ac[1][1]));
-        const float2 t2 = __ffma2_rn(my_c2, make_float2(ac[2][2], ac[2][3]), make_float2(ac[2][0], ac[2][1]));
-        const float2 t3 = __ffma2_rn(my_c2, make_float2(ac[3][2], ac[3][3]), make_float2(ac[3][0], ac[3][1]));
+        // rows g (hi) + g+8 (lo) of each group, then the groups' K scales
+        const float2 t0 = __fadd2_rn(make_float2(ac[0][0], ac[0][1]), make_float2(ac[0][2], ac[0][3]));
+        const float2 t1 = __fadd2_rn(make_float2(ac[1][0], ac[1][1]), make_float2(ac[1][2], ac[1][3]));
+        const float2 t2 = __fadd2_rn(make_float2(ac[2][0], ac[2][1]), make_float2(ac[2][2], ac[2][3]));
+        const float2 t3 = __fadd2_rn(make_float2(ac[3][0], ac[3][1]), make_float2(ac[3][2], ac[3][3]));
         const float2 v01 = __ffma2_rn(make_float2(s01.z, s01.w), t1, __fmul2_rn(make_float2(s01.x, s01.y), t0));
         const float2 v23 = __ffma2_rn(make_float2(s23.z, s23.w), t3, __fmul2_rn(make_float2(s23.x, s23.y), t2));
         float2 v = __fmul2_rn(__fadd2_rn(v01, v23), make_float2(my_c, my_c));
@@ -556,39 +524,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_fp4_mma_kernel(DecodeArgs 
     // V codes widen exactly to f16; the V scale 2^(e_v - Eref_G) multiplies the
     // P fragments of group G instead (two tokens per f16x2, as in the A fragment).
     const uint8_t* vbase = stg + kPagesPerChunk * kBlkStride + t * kVStride;
-    uint2 rA[8], rB[8];
-#pragma unroll
-    for (int jt = 0; jt < 8; ++jt) {
-      rA[jt] = *reinterpret_cast<const uint2*>(vbase + (16 * jt + g) * (kPage / 2));
-      rB[jt] = *reinterpret_cast<const uint2*>(vbase + (16 * jt + g + 8) * (kPage / 2));
-    }
     const uint32_t* vrow = vtab + t * (kVTabPage / 4);
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      // bytes 2c4 (tokens 4c4, 4c4+1) and 2c4+1 (tokens 4c4+2, 4c4+3)
-      const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
-      uint32_t xa[8][4], pgh[4][2], pgl[4][2];
+    for (int G4 = 0; G4 < 4; ++G4) {
+      const uint2 rA0 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + g) * (kPage / 2));
+      const uint2 rB0 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + g + 8) * (kPage / 2));
+      const uint2 rA1 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + 16 + g) * (kPage / 2));
+      const uint2 rB1 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + 16 + g + 8) * (kPage / 2));
+      const uint4 vs0 = *reinterpret_cast<const uint4*>(vrow + G4 * 8);
+      const uint4 vs1 = *reinterpret_cast<const uint4*>(vrow + G4 * 8 + 4);
+      const uint32_t vsc[8] = {vs0.x, vs0.y, vs0.z, vs0.w, vs1.x, vs1.y, vs1.z, vs1.w};
 #pragma unroll
-      for (int G4 = 0; G4 < 4; ++G4) {
-        const uint2 vs = *reinterpret_cast<const uint2*>(vrow + G4 * 8 + 2 * c4);
-        pgh[G4][0] = hmul2(ph[c4][0], vs.x);
-        pgh[G4][1] = hmul2(ph[c4][1], vs.y);
-        pgl[G4][0] = hmul2(pl[c4][0], vs.x);
-        pgl[G4][1] = hmul2(pl[c4][1], vs.y);
-      }
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt) {
-        const uint32_t wA = c4 < 2 ? rA[jt].x : rA[jt].y, wB = c4 < 2 ? rB[jt].x : rB[jt].y;
-        xa[jt][0] = e2m1x2_to_f16x2(wA, b0);
-        xa[jt][1] = e2m1x2_to_f16x2(wB, b0);
-        xa[jt][2] = e2m1x2_to_f16x2(wA, b1);
-        xa[jt][3] = e2m1x2_to_f16x2(wB, b1);
-        mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], pgh[jt >> 1][0], pgh[jt >> 1][1]);
-      }
-      if (need_lo[c4]) {
-#pragma unroll
-        for (int jt = 0; jt < 8; ++jt)
-          mma_f16(o[jt], xa[jt][0], xa[jt][1], xa[jt][2], xa[jt][3], pgl[jt >> 1][0], pgl[jt >> 1][1]);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
+        const uint32_t ph0 = hmul2(ph[c4][0], vsc[2 * c4]), ph1 = hmul2(ph[c4][1], vsc[2 * c4 + 1]);
+        const uint32_t wA0 = c4 < 2 ? rA0.x : rA0.y, wB0 = c4 < 2 ? rB0.x : rB0.y;
+        const uint32_t wA1 = c4 < 2 ? rA1.x : rA1.y, wB1 = c4 < 2 ? rB1.x : rB1.y;
+        const uint32_t x00 = e2m1x2_to_f16x2(wA0, b0), x01 = e2m1x2_to_f16x2(wB0, b0);
+        const uint32_t x02 = e2m1x2_to_f16x2(wA0, b1), x03 = e2m1x2_to_f16x2(wB0, b1);
+        const uint32_t x10 = e2m1x2_to_f16x2(wA1, b0), x11 = e2m1x2_to_f16x2(wB1, b0);
+        const uint32_t x12 = e2m1x2_to_f16x2(wA1, b1), x13 = e2m1x2_to_f16x2(wB1, b1);
+        mma_f16(o[2 * G4], x00, x01, x02, x03, ph0, ph1);
+        mma_f16(o[2 * G4 + 1], x10, x11, x12, x13, ph0, ph1);
+        if (need_lo[c4]) {
+          const uint32_t pl0 = hmul2(pl[c4][0], vsc[2 * c4]), pl1 = hmul2(pl[c4][1], vsc[2 * c4 + 1]);
+          mma_f16(o[2 * G4], x00, x01, x02, x03, pl0, pl1);
+          mma_f16(o[2 * G4 + 1], x10, x11, x12, x13, pl0, pl1);
+        }
       }
     }
     __syncwarp();
