@@ -26,7 +26,7 @@
 // online-softmax state, and merge at the end.  Each warp streams its chunks
 // with 1-D bulk copies (TMA, cp.async.bulk) into private shared-memory stages
 // completed through mbarriers, refilling a stage as soon as it is consumed.
-// Three CTAs share an SM (registers capped at 168 per thread), so twelve
+// Four CTAs share an SM (registers capped at 128 per thread), so sixteen
 // warps' copies and math overlap; one stage per warp measured faster than
 // two stages at two CTAs per SM.  Every wait is bounded: on timeout the
 // kernel flags KV4_DEVERR_TIMEOUT and stops.
@@ -113,13 +113,25 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One byte of two E2M1 codes -> f16x2 (low nibble -> low half), exact.
+// One byte of two E2M1 codes -> f16x2 (low nibble -> low half), exact.  The
+// word is split into .b8 registers so the conversion reads the byte lane in
+// place (a shift per byte otherwise); `byte` is a compile-time constant.
+#define KV4_CVT_BYTE(B)                                                              \
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"         \
+      "cvt.rn.f16x2.e2m1x2 %0, b" #B ";\n\t}"                                      \
+      : "=r"(out)                                                                    \
+      : "r"(word))
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t word, int byte) {
   uint32_t out;
-  const uint32_t b = word >> (8 * byte);
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(out) : "r"(b));
+  switch (byte) {
+    case 0: KV4_CVT_BYTE(0); break;
+    case 1: KV4_CVT_BYTE(1); break;
+    case 2: KV4_CVT_BYTE(2); break;
+    default: KV4_CVT_BYTE(3); break;
+  }
   return out;
 }
+#undef KV4_CVT_BYTE
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -166,7 +178,7 @@ struct Smem {
 // Rows: the R = T*G query rows of one kv head, R <= 8 (row r -> position
 // r / G, query head h*G + r % G); unused rows carry zero q and are never
 // written.
-__global__ void __launch_bounds__(kThreads, 3) decode_fp4_mma_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem sm{smem_raw};
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -353,17 +365,19 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp4_mma_kernel(DecodeArgs 
       }
       // V reference exponent per group (Eref): fixed from the warp's first
       // chunk, so the usual chunk needs no reduction.  The f16 scale factors
-      // 2^(e_v - Eref) hold exponents from -24 to +15; a chunk with an exponent
-      // more than 15 above Eref (a rare jump) raises Eref to the chunk maximum
-      // and the accumulators are rescaled below.
+      // 2^(e_v - Eref) hold exponents from -14 to +7; a chunk with an exponent
+      // more than 7 above Eref (a rare jump) raises Eref to the chunk maximum
+      // and the accumulators are rescaled below.  With p <= 2^8 (lazy softmax
+      // maximum) the scaled P stays below 2^15, inside the f16 range.
       eold = eref;
-      const uint32_t lim = __vaddus4(eref, 0x0F0F0F0Fu);
+      uint32_t lim = __vaddus4(eref, 0x07070707u);
       const bool over = (__vcmpgtu4(v0, lim) | __vcmpgtu4(v1, lim)) != 0u;
       if (it == 0 || __any_sync(0xffffffffu, over)) {
         uint32_t cm = __vmaxu4(v0, v1);
 #pragma unroll
         for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
         eref = __vmaxu4(eref, cm);
+        lim = __vaddus4(eref, 0x07070707u);
       }
       // K scale pairs: {2^e(tk,G), 2^e(tk+1,G)} for G = 0..3 (byte 0 -> 0.0)
       float4 f01, f23;
@@ -379,11 +393,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp4_mma_kernel(DecodeArgs 
       kt[0] = f01;
       kt[1] = f23;
       // V scale pairs 2^(e_v - Eref_G) as f16x2 (token tk low half, tk+1 high half):
-      // f16 exponent field 15 + e_v - Eref per byte, in [0, 30] here; values
+      // f16 exponent field 15 + e_v - Eref per byte, in [0, 22] here (as
+      // 22 - (Eref + 7 - e_v), both differences non-negative); values
       // below 2^-14 of the reference flush to zero.  A zero scale byte belongs
       // to an all-zero-code group, whose values are zero whatever the scale.
-      const uint32_t a0 = __vsubus4(__vaddus4(v0, 0x0F0F0F0Fu), eref);
-      const uint32_t a1 = __vsubus4(__vaddus4(v1, 0x0F0F0F0Fu), eref);
+      const uint32_t a0 = __vsubus4(0x16161616u, __vsubus4(lim, v0));
+      const uint32_t a1 = __vsubus4(0x16161616u, __vsubus4(lim, v1));
       uint4 vp;
       vp.x = __byte_perm(__byte_perm(a0, a1, 0x0040), 0, 0x5140) << 10;
       vp.y = __byte_perm(__byte_perm(a0, a1, 0x0051), 0, 0x5140) << 10;
@@ -461,7 +476,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp4_mma_kernel(DecodeArgs 
     float cmx = mx8[0];
     cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
     cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
-    const float m_new = fmaxf(m_run, cmx);
+    // Lazy maximum: the row's reference moves only when the chunk maximum
+    // exceeds it by more than 8 (log2 units), so p <= 2^8 and O is rarely
+    // rescaled.  Any reference gives the same (O, l) up to that common factor.
+    const float m_new = cmx > m_run + 8.0f ? cmx : m_run;
     float alpha = 1.0f;
     float2 p[8];
     if (m_new == -INFINITY) {
