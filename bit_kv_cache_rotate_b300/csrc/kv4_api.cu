@@ -189,6 +189,8 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   cudaError_t e;
   if (!fp8 && kv4::fast_path_supported(D, G, T, latent)) {
     e = kv4::launch_decode_fast(D, a, st);
+  } else if (fp8 && kv4::fp8_fast_path_supported(D, G, T)) {
+    e = kv4::launch_decode_fp8_fast(a, st);
   } else {
     if (T * G > kv4::ref_max_rows(D)) return KV4_ERR_UNSUPPORTED;
     e = kv4::launch_decode_ref(fp8, D, a, st);

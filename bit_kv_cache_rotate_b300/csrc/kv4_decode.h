@@ -23,9 +23,10 @@ struct DecodeArgs {
   float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
 };
 
-// Splits per sequence: about seven waves of two CTAs per SM (short waves keep
-// the tail small, more splits add partial-output traffic), at least four
-// pages per split.
+// Splits per sequence: about fourteen CTAs per SM in all (3.5 waves of the
+// 4-bit kernel's four resident CTAs; measured best at batch 32, 32K context,
+// where more splits add partial-output traffic and per-CTA set-up), at least
+// four pages per split.
 inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
   (void)head_dim;
   const int target = 14 * sms;
@@ -39,5 +40,7 @@ inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
 cudaError_t launch_decode_ref(bool fp8, int D, const DecodeArgs& a, cudaStream_t st);
 bool fast_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st);
+bool fp8_fast_path_supported(int D, int G, int T);
+cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st);
 
 }  // namespace kv4

@@ -34,9 +34,12 @@
 
 #include "kv4_common.cuh"
 #include "kv4_decode.h"
+#include "kv4_mma_common.cuh"
 
 namespace kv4 {
 namespace fast {
+
+using namespace kv4::mma;
 
 constexpr int D = 128;
 constexpr int kWarps = 4;
@@ -57,110 +60,6 @@ constexpr int kTabBytes = kKTab + kVTab;
 constexpr int kQBytes = 8 * 2 * D * 2;             // f16 q [8 rows][hi, lo][128 ch], aliases the tables
 static_assert(kWarps * kTabBytes >= kQBytes, "q terms must fit in the table area");
 constexpr int kSmem = kWarps * kStages * kStageBytes + kWarps * kTabBytes + 8 * kWarps * kStages;
-constexpr int kSpinLimit = 1 << 16;     // try_wait rounds, each suspending up to kSuspendNs
-constexpr uint32_t kSuspendNs = 20000;
-
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-// Bounded wait for the phase with the given parity; false on timeout.  The
-// suspend hint lets a waiting warp sleep instead of spinning on issue slots.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  for (int i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(addr), "r"(parity), "r"(kSuspendNs)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// One byte of two E2M1 codes -> f16x2 (low nibble -> low half), exact.  The
-// word is split into .b8 registers so the conversion reads the byte lane in
-// place (a shift per byte otherwise); `byte` is a compile-time constant.
-#define KV4_CVT_BYTE(B)                                                              \
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"         \
-      "cvt.rn.f16x2.e2m1x2 %0, b" #B ";\n\t}"                                      \
-      : "=r"(out)                                                                    \
-      : "r"(word))
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t word, int byte) {
-  uint32_t out;
-  switch (byte) {
-    case 0: KV4_CVT_BYTE(0); break;
-    case 1: KV4_CVT_BYTE(1); break;
-    case 2: KV4_CVT_BYTE(2); break;
-    default: KV4_CVT_BYTE(3); break;
-  }
-  return out;
-}
-#undef KV4_CVT_BYTE
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t d;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  return d;
-}
-
-// Split a pair x >= 0 into f16-exact hi parts (11 significant bits, Veltkamp)
-// and the remainders.  Packed fp32x2 ops with explicit rounding: no step can
-// be contracted into an FMA, which would break the split.
-__device__ __forceinline__ void split_hi_lo2(float2 x, float2& hi, float2& lo) {
-  const float2 m1 = make_float2(-1.0f, -1.0f);
-  const float2 c = __fmul2_rn(x, make_float2(8193.0f, 8193.0f));
-  const float2 t = __ffma2_rn(x, m1, c);   // c - x
-  hi = __ffma2_rn(t, m1, c);               // c - (c - x)
-  lo = __ffma2_rn(hi, m1, x);              // x - hi (exact)
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 struct Smem {
   uint8_t* base;

@@ -199,3 +199,51 @@ def test_fp8_append_and_decode_parity(name):
                                       lay.context_lens, cfg.num_kv_heads, cfg.page_size, lay.num_pages,
                                       cfg.softmax_scale)
     assert np.abs(out.cpu().numpy() - ref).max() <= TOL
+
+
+@pytest.mark.parametrize("ctx", [1, 2, 15, 16, 17, 63, 64, 65, 127, 255, 257, 1021])
+def test_decode_single_query_ragged_contexts(ctx):
+    # T = 1, G = 8: the tensor-core kernel, with partial pages, partial chunks
+    # and splits that end mid-chunk
+    cfg = W.scaled(W.CONFIGS["b32_ctx8k"], batch=3, ctx=("fixed", ctx))
+    lay = W.make_layout(cfg)
+    k, v, slots = all_tokens(cfg, lay)
+    okc, ovc = oracle_caches(cfg, lay, k, v, slots)
+    gkc, gvc = gpu_caches(kv4, cfg, lay, k, v, slots)
+    q = W.queries(cfg)
+    for S in (1, 3):
+        got, ref = _decode_pair(cfg, lay, okc, ovc, gkc, gvc, q, num_splits=S)
+        assert np.abs(got - ref).max() <= TOL, S
+
+
+def _fp8_pair(cfg, num_splits=0):
+    lay, okc, ovc, gkc, gvc, ks, vs = _fp8_setup(cfg)
+    q = W.queries(cfg)
+    tab, lens = gpu_tables(lay)
+    out = kv4.fp8_decode_attention(q.cuda(), gkc, gvc, torch.from_numpy(ks).cuda(),
+                                   torch.from_numpy(vs).cuda(), tab, lens, cfg.num_kv_heads,
+                                   lay.num_pages, cfg.softmax_scale, num_splits=num_splits)
+    torch.cuda.synchronize()
+    ref = oracle.fp8_decode_attention(q, okc, ovc, ks, vs, np.where(lay.block_tables < 0, 0, lay.block_tables),
+                                      lay.context_lens, cfg.num_kv_heads, cfg.page_size, lay.num_pages,
+                                      cfg.softmax_scale)
+    return out.cpu().numpy().astype(np.float64), ref
+
+
+def test_fp8_split_count_invariance_and_tiny():
+    outs = []
+    for S in (1, 2, 5, 63):
+        got, ref = _fp8_pair(SMALL["b32_small"], num_splits=S)
+        assert np.abs(got - ref).max() <= TOL, S
+        outs.append(got)
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 1e-4
+    got, ref = _fp8_pair(SMALL["tiny"])  # G = 4, outlier channels x20
+    assert np.abs(got - ref).max() <= TOL
+
+
+@pytest.mark.parametrize("ctx", [1, 15, 17, 64, 65, 257])
+def test_fp8_single_query_ragged_contexts(ctx):
+    cfg = W.scaled(W.CONFIGS["b32_ctx8k"], batch=2, ctx=("fixed", ctx))
+    got, ref = _fp8_pair(cfg, num_splits=2)
+    assert np.abs(got - ref).max() <= TOL
