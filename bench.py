@@ -43,7 +43,8 @@ from bit_kv_cache_rotate_b300 import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6400.0
 DECODE_SOURCES = ("bit_kv_cache_rotate_b300/csrc/kv4_decode_mma.cu",
-                  "bit_kv_cache_rotate_b300/csrc/kv4_decode_ref.cu")
+                  "bit_kv_cache_rotate_b300/csrc/kv4_mma_common.cuh",
+                  "bit_kv_cache_rotate_b300/csrc/kv4_decode.h")
 METRIC = "4-bit-KV decode attention: HBM GB/s (% of peak) and ms/step at 32K ctx, batch 32"
 
 
