@@ -1,6 +1,7 @@
 // kv4_api.cu -- host side of libkv4: argument validation, split choice and
 // kernel dispatch behind the extern "C" entry points declared in kv4.h.
 #include <math.h>
+#include <stdlib.h>
 
 #include "kv4_common.cuh"
 
@@ -187,9 +188,19 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   a.qscale = (float)(softmax_scale * log2e * (fp8 ? 1.0 : inv_sqrt_dim(D)));
 
   cudaError_t e;
-  if (!fp8 && kv4::fast_path_supported(D, G, T, latent)) {
+  // The warp-MMA kernel is the default tensor-core path; the tcgen05 block-
+  // scaled kernel serves the same shapes when KV4_DECODE_TCGEN05=1 (it was
+  // measured slower at batch 32, 32K context).
+  const char* tc_env = getenv("KV4_DECODE_TCGEN05");
+  const bool use_tc = tc_env != nullptr && tc_env[0] == '1';
+  a.pos_split = 0;
+  if (!fp8 && use_tc && kv4::tc_path_supported(D, G, T, latent)) {
+    e = kv4::launch_decode_tc(a, st);
+  } else if (!fp8 && kv4::fast_path_supported(D, G, T, latent)) {
+    a.pos_split = T * G > 8 ? 1 : 0;
     e = kv4::launch_decode_fast(D, a, st);
   } else if (fp8 && kv4::fp8_fast_path_supported(D, G, T)) {
+    a.pos_split = T * G > 8 ? 1 : 0;
     e = kv4::launch_decode_fp8_fast(a, st);
   } else {
     if (T * G > kv4::ref_max_rows(D)) return KV4_ERR_UNSUPPORTED;

@@ -82,8 +82,9 @@ __global__ void __launch_bounds__(256) append_fp4_kernel(
   for (int i = 0; i < E; i += 2) byte[i / 2] = f32x2_to_e2m1x2(y[i] * inv, y[i + 1] * inv);
 
   if (which == 0) {
-    // K: token-major codes, lane's E channels are E/2 consecutive bytes.
-    uint8_t* dst = blk + off * (D / 2) + lane * (E / 2);
+    // K: 8-token x 32-channel tiles; the lane's E channels (E <= 16, aligned)
+    // stay inside one tile row, E/2 consecutive bytes.
+    uint8_t* dst = blk + k_code_offset(D, off, lane * E);
     if constexpr (E == 2) {
       dst[0] = (uint8_t)byte[0];
     } else if constexpr (E == 4) {

@@ -56,6 +56,13 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
 }
 
 // Two E4M3 bytes (lo in bits 7:0) -> two fp32 values (exact).
+// Byte offset of (token t, channel d) in a K code plane: tiles of 8 tokens x
+// 32 channels, 128 bytes each, tile (t/8, d/32) at ((t/8)*(D/32) + d/32)*128,
+// token t%8 at +16*(t%8), channel d in byte (d%32)/2 (low nibble even).
+__host__ __device__ __forceinline__ int k_code_offset(int D, int t, int d) {
+  return ((t >> 3) * (D >> 5) + (d >> 5)) * 128 + (t & 7) * 16 + ((d & 31) >> 1);
+}
+
 __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));

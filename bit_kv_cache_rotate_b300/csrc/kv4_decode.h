@@ -20,6 +20,7 @@ struct DecodeArgs {
   int32_t* dev_error;
   int B, T, Hq, Hkv, max_pages, num_pages, S;
   int latent;
+  int pos_split;           // 1: one CTA per query position (grid z = B * T)
   float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
 };
 
@@ -40,6 +41,8 @@ inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
 cudaError_t launch_decode_ref(bool fp8, int D, const DecodeArgs& a, cudaStream_t st);
 bool fast_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st);
+bool tc_path_supported(int D, int G, int T, bool latent);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 bool fp8_fast_path_supported(int D, int G, int T);
 cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st);
 

@@ -43,13 +43,20 @@ static_assert(kWarps * kStageBytes >= kWarps * 8 * D * 4 + 2 * kWarps * 8 * 4, "
 
 __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
+  // position j of the sequence; position j attends to the first L - T + 1 + j
+  // tokens (causal verify), i.e. a single-position decode over that prefix.
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int b = a.pos_split ? (int)blockIdx.z / a.T : (int)blockIdx.z;
+  const int j0 = a.pos_split ? (int)blockIdx.z % a.T : 0;
+  const int Tc = a.pos_split ? 1 : a.T;  // query positions in this CTA
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int G = a.Hq / a.Hkv;
-  const int R = a.T * G;
-  const int L = a.context_lens[b];
-  const size_t row0 = (size_t)b * a.T * a.Hq;
+  const int R = Tc * G;
+  const int L_seq = a.context_lens[b];
+  const int L = L_seq - (a.T - Tc) + j0;  // tokens visible to this CTA's last position
+  const size_t row0 = ((size_t)b * a.T + j0) * a.Hq;
   uint8_t* stage = smem_raw + w * kStageBytes;
   uint16_t* qt = reinterpret_cast<uint16_t*>(smem_raw + kWarps * kStageBytes);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + kWarps * kStageBytes + kQBytes) + w;
@@ -62,7 +69,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
       if (lane == 0) a.part_lse[rr] = -INFINITY;
     }
   };
-  if (L < a.T || L > a.max_pages * kPage) {
+  if (L_seq < a.T || L_seq > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
     return;
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
     if (lane == 0) {
       // score*log2e = (q*2^sigma . k_e4m3) * 2^-sigma * k_scale * softmax_scale*log2e
       row_c[r] = a.qscale * a.k_scale[h] * __uint_as_float((uint32_t)(127 - sigma) << 23);
-      row_limit[r] = r < R ? L - a.T + 1 + r / G : 0x7fffffff;
+      row_limit[r] = r < R ? L - Tc + 1 + r / G : 0x7fffffff;
     }
   }
   __syncthreads();
@@ -383,7 +390,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
 
 }  // namespace fp8fast
 
-bool fp8_fast_path_supported(int D, int G, int T) { return D == 128 && T * G <= 8; }
+bool fp8_fast_path_supported(int D, int G, int T) {
+  (void)T;  // T * G > 8 runs one CTA per query position (pos_split)
+  return D == 128 && G <= 8;
+}
 
 cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st) {
   static bool attr = false;
@@ -393,7 +403,7 @@ cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const dim3 grid(a.S, a.Hkv, a.B);
+  const dim3 grid(a.S, a.Hkv, a.B * (a.pos_split ? a.T : 1));
   fp8fast::decode_fp8_mma_kernel<<<grid, fp8fast::kThreads, fp8fast::kSmem, st>>>(a);
   return cudaGetLastError();
 }

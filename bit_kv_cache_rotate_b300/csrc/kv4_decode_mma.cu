@@ -80,13 +80,20 @@ struct Smem {
 __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem sm{smem_raw};
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
+  // position j of the sequence; position j attends to the first L - T + 1 + j
+  // tokens (causal verify), i.e. a single-position decode over that prefix.
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int b = a.pos_split ? (int)blockIdx.z / a.T : (int)blockIdx.z;
+  const int j0 = a.pos_split ? (int)blockIdx.z % a.T : 0;
+  const int Tc = a.pos_split ? 1 : a.T;  // query positions in this CTA
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int G = a.Hq / a.Hkv;
-  const int R = a.T * G;
-  const int L = a.context_lens[b];
-  const size_t row0 = (size_t)b * a.T * a.Hq;
+  const int R = Tc * G;
+  const int L_seq = a.context_lens[b];
+  const int L = L_seq - (a.T - Tc) + j0;  // tokens visible to this CTA's last position
+  const size_t row0 = ((size_t)b * a.T + j0) * a.Hq;
 
   auto row_index = [&](int r) -> size_t {  // flat (b, j, hq) row of query row r
     return row0 + (size_t)(r / G) * a.Hq + h * G + (r % G);
@@ -98,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
       if (lane == 0) a.part_lse[rr] = -INFINITY;
     }
   };
-  if (L < a.T || L > a.max_pages * kPage) {
+  if (L_seq < a.T || L_seq > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
     return;
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
     if (lane == 0) {
       // score*log2e = (q*2^sigma . code * 2^e) * 2^-sigma * softmax_scale*log2e/sqrt(D)
       row_c[r] = a.qscale * __uint_as_float((uint32_t)(127 - sigma) << 23);
-      row_limit[r] = r < R ? L - a.T + 1 + r / G : 0x7fffffff;
+      row_limit[r] = r < R ? L - Tc + 1 + r / G : 0x7fffffff;
     }
   }
   __syncthreads();
@@ -324,10 +331,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
       uint32_t kb[2][4][4];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const uint8_t* krow = stg + (g >> 1) * kBlkStride + (2 * (n + u) + (g & 1)) * (D / 2) + 4 * t;
+        const uint8_t* krow = stg + (g >> 1) * kBlkStride + k_code_offset(D, 2 * (n + u) + (g & 1), 8 * t);
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
-          const uint32_t x = *reinterpret_cast<const uint32_t*>(krow + 16 * G4);
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(krow + 128 * G4);
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) kb[u][G4][bb] = e2m1x2_to_f16x2(x, bb);
         }
@@ -536,7 +543,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
 }  // namespace fast
 
 bool fast_path_supported(int D, int G, int T, bool latent) {
-  return D == 128 && !latent && T * G <= 8;
+  (void)T;  // T * G > 8 runs one CTA per query position (pos_split)
+  return D == 128 && !latent && G <= 8;
 }
 
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
@@ -548,7 +556,7 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const dim3 grid(a.S, a.Hkv, a.B);
+  const dim3 grid(a.S, a.Hkv, a.B * (a.pos_split ? a.T : 1));
   fast::decode_fp4_mma_kernel<<<grid, fast::kThreads, fast::kSmem, st>>>(a);
   return cudaGetLastError();
 }

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kRefThreads) decode_ref_kernel(DecodeArgs a) {
         vv = e4m3x2_to_f32x2(vb[d * kPage + t]).x * vsc;
       } else {
         const uint8_t* ksb = kb + kPage * D / 2;
-        const uint32_t kc = (kb[t * (D / 2) + d / 2] >> ((d & 1) * 4)) & 0xFu;
+        const uint32_t kc = (kb[k_code_offset(D, t, d)] >> ((d & 1) * 4)) & 0xFu;
         kv = e2m1_to_float(kc) * ue8m0_to_float(ksb[t * (D / 32) + d / 32]);
         if (a.latent) {
           vv = kv;

@@ -32,8 +32,11 @@
  * Cache layout (one block per (page, kv head), blocks page-major:
  * block index = page * num_kv_heads + head, block bytes = P*D/2 + P*D/32):
  *   K block (also the latent cache):
- *     codes  [P][D/2]  token-major: byte (t, j) = channel 2j (low nibble),
- *                      channel 2j+1 (high nibble) of token t
+ *     codes  tiles of 8 tokens x 32 channels (128 bytes): tile (t/8, d/32)
+ *            starts at byte ((t/8)*(D/32) + d/32)*128; inside it token t%8
+ *            takes 16 bytes, byte (d%32)/2 holding channel d (low nibble =
+ *            even channel).  This is the 8-row core-matrix order in which
+ *            the block-scaled tensor-core MMA reads its K operand.
  *     scales [P][D/32] one UE8M0 byte (exponent + 127) per (token, group)
  *   V block:
  *     codes  [D][P/2]  channel-major: byte (d, j) = token 2j (low nibble),

@@ -247,8 +247,11 @@ int orc_quantize_vector(const uint16_t* x, int D, uint8_t* codes, int* expo) {
 /* R6: block layout.  One block per (page, kv head); blocks are stored  */
 /* page-major: block index = page * num_kv_heads + head.                */
 /*   K block (also the latent cache):                                   */
-/*     codes  [P][D/2]  token-major; byte (t, j) holds channel 2j in    */
-/*                      the low nibble, channel 2j+1 in the high nibble */
+/*     codes  in tiles of 8 tokens x 32 channels, 128 bytes each, tile  */
+/*            (t/8, d/32) at byte ((t/8)*(D/32) + d/32)*128; inside a   */
+/*            tile token t%8 takes 16 bytes and byte (d%32)/2 holds     */
+/*            channel d, low nibble = even channel.  (This is the order */
+/*            a block-scaled tensor-core MMA reads 8-row tiles in.)     */
 /*     scales [P][D/32] UE8M0 byte per (token, 32-channel group)        */
 /*   V block:                                                           */
 /*     codes  [D][P/2]  channel-major; byte (d, j) holds token 2j in    */
@@ -269,10 +272,14 @@ static int get_nibble(uint8_t byte, int high) {
   return high ? (byte >> 4) & 0xF : byte & 0xF;
 }
 
+/* Byte of (token t, channel d) in a K code plane (R6). */
+static size_t k_code_byte(int D, int t, int d) {
+  return ((size_t)(t / 8) * (D / 32) + d / 32) * 128 + (size_t)(t % 8) * 16 + (d % 32) / 2;
+}
+
 void orc_pack_k_token(uint8_t* block, int page_size, int D, int off,
                       const uint8_t* codes, const int* expo) {
-  uint8_t* c = block + (size_t)off * (D / 2);
-  for (int d = 0; d < D; ++d) put_nibble(&c[d / 2], d & 1, codes[d]);
+  for (int d = 0; d < D; ++d) put_nibble(&block[k_code_byte(D, off, d)], d & 1, codes[d]);
   uint8_t* s = block + (size_t)page_size * D / 2 + (size_t)off * (D / 32);
   for (int g = 0; g < D / 32; ++g) s[g] = (uint8_t)(expo[g] + 127);
 }
@@ -289,10 +296,9 @@ void orc_pack_v_token(uint8_t* block, int page_size, int D, int off,
 
 /* Dequantised (still rotated) value of one cached token, fp64, exact. */
 void orc_unpack_k_token(const uint8_t* block, int page_size, int D, int off, double* out) {
-  const uint8_t* c = block + (size_t)off * (D / 2);
   const uint8_t* s = block + (size_t)page_size * D / 2 + (size_t)off * (D / 32);
   for (int d = 0; d < D; ++d) {
-    int code = get_nibble(c[d / 2], d & 1);
+    int code = get_nibble(block[k_code_byte(D, off, d)], d & 1);
     out[d] = ldexp(orc_e2m1_decode(code), (int)s[d / 32] - 127);
   }
 }

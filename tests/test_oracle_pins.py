@@ -201,8 +201,9 @@ def test_format_bytes_golden():
 
 
 def test_block_layout_positions():
-    """Codes/scales land where the layout says: K token-major low-nibble-even
-    channel, V channel-major low-nibble-even token, scales after the codes."""
+    """Codes/scales land where the layout says: K in 8-token x 32-channel tiles
+    of 128 bytes (16 bytes per token, low nibble = even channel), V
+    channel-major low-nibble-even token, scales after the codes."""
     P, D, Hkv = 16, 128, 2
     bb = oracle.block_bytes(P, D)
     rng = np.random.default_rng(2)
@@ -219,7 +220,7 @@ def test_block_layout_positions():
         for h in range(Hkv):
             base = (page * Hkv + h) * bb
             for d in range(D):
-                kb = kc[base + off * (D // 2) + d // 2]
+                kb = kc[base + ((off // 8) * (D // 32) + d // 32) * 128 + (off % 8) * 16 + (d % 32) // 2]
                 assert ((kb >> 4) if d & 1 else (kb & 15)) == kcodes[i, h, d]
                 vb = vc[base + d * (P // 2) + off // 2]
                 assert ((vb >> 4) if off & 1 else (vb & 15)) == vcodes[i, h, d]
