@@ -196,6 +196,8 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   a.pos_split = 0;
   if (!fp8 && use_tc && kv4::tc_path_supported(D, G, T, latent)) {
     e = kv4::launch_decode_tc(a, st);
+  } else if (!fp8 && kv4::mla_path_supported(D, G, T, latent)) {
+    e = kv4::launch_decode_mla(a, st);
   } else if (!fp8 && kv4::fast_path_supported(D, G, T, latent)) {
     a.pos_split = T * G > 8 ? 1 : 0;
     e = kv4::launch_decode_fast(D, a, st);

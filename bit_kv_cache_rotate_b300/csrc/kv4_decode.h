@@ -28,9 +28,10 @@ struct DecodeArgs {
 // 4-bit kernel's four resident CTAs; measured best at batch 32, 32K context,
 // where more splits add partial-output traffic and per-CTA set-up), at least
 // four pages per split.
+// The latent (head_dim 512) kernel is compute-bound at two CTAs per SM:
+// about one wave, so the split partials stay small.
 inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
-  (void)head_dim;
-  const int target = 14 * sms;
+  const int target = head_dim == 512 ? 2 * sms : 14 * sms;
   int s = (target + units / 2) / units;
   const int cap = max_pages / 4 > 0 ? max_pages / 4 : 1;
   if (s > cap) s = cap;
@@ -41,6 +42,8 @@ inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
 cudaError_t launch_decode_ref(bool fp8, int D, const DecodeArgs& a, cudaStream_t st);
 bool fast_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st);
+bool mla_path_supported(int D, int G, int T, bool latent);
+cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st);
 bool tc_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 bool fp8_fast_path_supported(int D, int G, int T);

@@ -247,3 +247,22 @@ def test_fp8_single_query_ragged_contexts(ctx):
     cfg = W.scaled(W.CONFIGS["b32_ctx8k"], batch=2, ctx=("fixed", ctx))
     got, ref = _fp8_pair(cfg, num_splits=2)
     assert np.abs(got - ref).max() <= TOL
+
+
+@pytest.mark.parametrize("ctx", [("fixed", 1), ("fixed", 33), ("uniform", 17, 900), ("fixed", 2049)])
+def test_mla_latent_decode_ragged_and_split_invariant(ctx):
+    # D = 512 latent cache (K = V), 16 query rows per latent head: the latent kernel
+    cfg = W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=ctx)
+    lay = W.make_layout(cfg)
+    k, v, slots = all_tokens(cfg, lay)
+    okc, ovc = oracle_caches(cfg, lay, k, v, slots)
+    gkc, gvc = gpu_caches(kv4, cfg, lay, k, v, slots)
+    q = W.queries(cfg)
+    outs = []
+    for S in (1, 3, 7):
+        got, ref = _decode_pair(cfg, lay, okc, ovc, gkc, gvc, q, num_splits=S)
+        assert np.isfinite(got).all()
+        assert np.abs(got - ref).max() <= TOL, (S, np.abs(got - ref).max())
+        outs.append(got)
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 1e-4
