@@ -24,14 +24,14 @@ struct DecodeArgs {
   float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
 };
 
-// Splits per sequence: about fourteen CTAs per SM in all (3.5 waves of the
+// Splits per sequence: about seven CTAs per SM in all (1.75 waves of the
 // 4-bit kernel's four resident CTAs; measured best at batch 32, 32K context,
 // where more splits add partial-output traffic and per-CTA set-up), at least
 // four pages per split.
 // The latent (head_dim 512) kernel is compute-bound at two CTAs per SM:
 // about one wave, so the split partials stay small.
 inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
-  const int target = head_dim == 512 ? 2 * sms : 14 * sms;
+  const int target = head_dim == 512 ? 2 * sms : 7 * sms;
   int s = (target + units / 2) / units;
   const int cap = max_pages / 4 > 0 ? max_pages / 4 : 1;
   if (s > cap) s = cap;

@@ -47,8 +47,8 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kPagesPerChunk = 4;
 constexpr int kBlk = kPage * D / 2 + kPage * D / 32;  // 1088 bytes per (page, head) block
 constexpr int kCodeBytes = kPage * D / 2;            // 1024
-constexpr int kBlkStride = 1104;                     // smem stride between staged K blocks (bank spread)
-constexpr int kVStride = 1120;                       // smem stride between staged V blocks (bank spread)
+constexpr int kBlkStride = 1088;                     // smem stride between staged K blocks
+constexpr int kVStride = 1104;                       // smem stride between staged V blocks (bank spread)
 constexpr int kStageBytes = kPagesPerChunk * (kBlkStride + kVStride);  // K blocks then V blocks
 constexpr int kStages = 1;
 // Scale tables, rows padded so the four t-lanes of a quad hit distinct banks.
@@ -59,7 +59,10 @@ constexpr int kVTab = kPagesPerChunk * kVTabPage;
 constexpr int kTabBytes = kKTab + kVTab;
 constexpr int kQBytes = 8 * 2 * D * 2;             // f16 q [8 rows][hi, lo][128 ch], aliases the tables
 static_assert(kWarps * kTabBytes >= kQBytes, "q terms must fit in the table area");
-constexpr int kSmem = kWarps * kStages * kStageBytes + kWarps * kTabBytes + 8 * kWarps * kStages;
+// q A-fragments, [group][k-step][lane] uint4, read per use: keeping them in
+// registers (32 per thread) spilled at the 128-register cap of four CTAs/SM.
+constexpr int kQFragOff = kWarps * kStages * kStageBytes + kWarps * kTabBytes + 8 * kWarps * kStages;
+constexpr int kSmem = kQFragOff + 4 * 2 * 32 * 16;
 
 struct Smem {
   uint8_t* base;
@@ -211,14 +214,17 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
   // lo.  Step j's k index 2t+i maps to channel 32G + 8t + 4j + i and 2t+8+i to
   // 32G + 8t + 4j + 2 + i, matching the K B-fragments built from one 32-bit
   // word of codes per thread (bytes 4t .. 4t+3 of the group).
-  uint32_t qa[4][2][4];
+  uint4* qfrag = reinterpret_cast<uint4*>(smem_raw + kQFragOff);
+  if (w == 0) {
 #pragma unroll
-  for (int G4 = 0; G4 < 4; ++G4) {
-    const uint4 hi = *reinterpret_cast<const uint4*>(qt + (g * 2) * D + 32 * G4 + 8 * t);
-    const uint4 lo = *reinterpret_cast<const uint4*>(qt + (g * 2 + 1) * D + 32 * G4 + 8 * t);
-    qa[G4][0][0] = hi.x; qa[G4][0][1] = lo.x; qa[G4][0][2] = hi.y; qa[G4][0][3] = lo.y;
-    qa[G4][1][0] = hi.z; qa[G4][1][1] = lo.z; qa[G4][1][2] = hi.w; qa[G4][1][3] = lo.w;
+    for (int G4 = 0; G4 < 4; ++G4) {
+      const uint4 hi = *reinterpret_cast<const uint4*>(qt + (g * 2) * D + 32 * G4 + 8 * t);
+      const uint4 lo = *reinterpret_cast<const uint4*>(qt + (g * 2 + 1) * D + 32 * G4 + 8 * t);
+      qfrag[(G4 * 2 + 0) * 32 + lane] = make_uint4(hi.x, lo.x, hi.y, lo.y);
+      qfrag[(G4 * 2 + 1) * 32 + lane] = make_uint4(hi.z, lo.z, hi.w, lo.w);
+    }
   }
+  const uint32_t qfrag_addr = smem_u32(qfrag) + lane * 16;
   const float my_c = row_c[g];
   const int my_limit = row_limit[g];
   int min_limit = row_limit[0];
@@ -342,11 +348,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
 #pragma unroll
       for (int j2 = 0; j2 < 2; ++j2)
 #pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4)
+        for (int G4 = 0; G4 < 4; ++G4) {
+          uint32_t q0, q1, q2, q3;
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
+                       : "r"(qfrag_addr + (G4 * 2 + j2) * 512));
 #pragma unroll
           for (int u = 0; u < 2; ++u)
-            mma_f16(acc[u][G4], qa[G4][j2][0], qa[G4][j2][1], qa[G4][j2][2], qa[G4][j2][3],
-                    kb[u][G4][2 * j2], kb[u][G4][2 * j2 + 1]);
+            mma_f16(acc[u][G4], q0, q1, q2, q3, kb[u][G4][2 * j2], kb[u][G4][2 * j2 + 1]);
+        }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const float4* kt =
