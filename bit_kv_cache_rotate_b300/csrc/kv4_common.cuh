@@ -5,6 +5,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "kv4.h"
@@ -98,6 +100,21 @@ __device__ __forceinline__ void fwht_warp(T (&x)[E]) {
       x[i] = upper ? (o - x[i]) : (x[i] + o);
     }
   }
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once
+// per device (the attribute is per device); safe to call from several host
+// threads (the call is idempotent).
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel* kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 __device__ __forceinline__ void flag_error(int32_t* dev_error, int bit) {

@@ -396,13 +396,9 @@ bool fp8_fast_path_supported(int D, int G, int T) {
 }
 
 cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(fp8fast::decode_fp8_mma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, fp8fast::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(fp8fast::decode_fp8_mma_kernel, fp8fast::kSmem, smem_set);
+  if (e != cudaSuccess) return e;
   const dim3 grid(a.S, a.Hkv, a.B * (a.pos_split ? a.T : 1));
   fp8fast::decode_fp8_mma_kernel<<<grid, fp8fast::kThreads, fp8fast::kSmem, st>>>(a);
   return cudaGetLastError();

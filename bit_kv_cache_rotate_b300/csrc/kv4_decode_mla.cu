@@ -492,13 +492,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
 bool mla_path_supported(int D, int G, int T, bool latent) { return D == 512 && latent && T * G <= 16; }
 
 cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(mla::decode_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mla::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(mla::decode_mla_kernel, mla::kSmem, smem_set);
+  if (e != cudaSuccess) return e;
   const dim3 grid(a.S, a.Hkv, a.B);
   mla::decode_mla_kernel<<<grid, mla::kThreads, mla::kSmem, st>>>(a);
   return cudaGetLastError();

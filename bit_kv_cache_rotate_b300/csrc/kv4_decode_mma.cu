@@ -558,13 +558,9 @@ bool fast_path_supported(int D, int G, int T, bool latent) {
 
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
   if (D != 128) return cudaErrorNotSupported;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(fast::decode_fp4_mma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, fast::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel, fast::kSmem, smem_set);
+  if (e != cudaSuccess) return e;
   const dim3 grid(a.S, a.Hkv, a.B * (a.pos_split ? a.T : 1));
   fast::decode_fp4_mma_kernel<<<grid, fast::kThreads, fast::kSmem, st>>>(a);
   return cudaGetLastError();

@@ -639,13 +639,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_tc_kernel(DecodeArgs a
 bool tc_path_supported(int D, int G, int T, bool latent) { return D == 128 && !latent && T * G <= 8; }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tc::decode_fp4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(tc::decode_fp4_tc_kernel, tc::kSmem, smem_set);
+  if (e != cudaSuccess) return e;
   const dim3 grid(a.S, a.Hkv, a.B);
   tc::decode_fp4_tc_kernel<<<grid, tc::kThreads, tc::kSmem, st>>>(a);
   return cudaGetLastError();
