@@ -68,6 +68,21 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """Maximum of x over the ranks of the default process group (x when world == 1)."""
+    if world <= 1:
+        return x
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s of `world` independent replicas timed by the slowest rank."""
+    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -272,12 +287,9 @@ def run_ours(args, rank, world, local_rank):
     elapsed_ms = t0.elapsed_time(t1)
     kern_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     del graph
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
     ms_per_step = elapsed_ms / args.steps
-    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
+    value = replica_gbs(nbytes, world, ms_per_step)
 
     # ---- e2e through the public API with host buffers
     h_q = wl.q.cpu().pin_memory()
@@ -311,10 +323,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_s) + ((h_v,) if h_v is not None else ()))
     d2h = h_out.numel() * h_out.element_size()
 
@@ -376,7 +385,7 @@ def run_ours(args, rank, world, local_rank):
                      "peak": peak, "peak_kind": f"{peak_kind} (hbm copy)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": stored_traffic(cfg.name),
                      "kernel_ms": round(kern_ms, 5)},
-        "e2e": {"value": round(nbytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(replica_gbs(nbytes, world, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
