@@ -20,7 +20,7 @@ struct DecodeArgs {
   int32_t* dev_error;
   int B, T, Hq, Hkv, max_pages, num_pages, S;
   int latent;
-  int pos_split;           // 1: one CTA per query position (grid z = B * T)
+  int pos_split;           // 1: one CTA per query position (grid x = S * T)
   float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
 };
 

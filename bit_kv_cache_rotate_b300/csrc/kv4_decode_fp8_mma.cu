@@ -38,7 +38,9 @@ constexpr int kVStride = kBlk + 32;    // staged V blocks: +2 16-byte units so t
                                        // land on distinct banks
 constexpr int kStageBytes = kPagesPerChunk * (kKStride + kVStride);
 constexpr int kQBytes = 8 * 2 * D * 2;  // f16 q [8 rows][hi, lo][128 ch]
-constexpr int kSmem = kWarps * kStageBytes + kQBytes + 8 * kWarps;
+// q A-fragments [k-step][lane] uint4, read per use (registers would spill)
+constexpr int kOffQFrag = kWarps * kStageBytes + kQBytes + 8 * kWarps;
+constexpr int kSmem = kOffQFrag + 8 * 32 * 16;
 static_assert(kWarps * kStageBytes >= kWarps * 8 * D * 4 + 2 * kWarps * 8 * 4, "merge area must fit");
 
 __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs a) {
@@ -46,9 +48,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
   // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
   // position j of the sequence; position j attends to the first L - T + 1 + j
   // tokens (causal verify), i.e. a single-position decode over that prefix.
-  const int s = blockIdx.x, h = blockIdx.y;
-  const int b = a.pos_split ? (int)blockIdx.z / a.T : (int)blockIdx.z;
-  const int j0 = a.pos_split ? (int)blockIdx.z % a.T : 0;
+  // The T position-CTAs of one (split, head, sequence) are neighbours in
+  // launch order (x = split * T + position): they read the same pages, so the
+  // second and third reads are mostly served by L2.
+  const int s = a.pos_split ? (int)blockIdx.x / a.T : (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int j0 = a.pos_split ? (int)blockIdx.x % a.T : 0;
   const int Tc = a.pos_split ? 1 : a.T;  // query positions in this CTA
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -155,16 +160,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
   // A fragments for the eight k16 steps j: thread t covers channels 32t .. 32t+31;
   // k index 2t+i of step j is channel 32t + 4j + i, 2t+8+i is 32t + 4j + 2 + i,
   // matching the K words (4 channels per 32-bit word) read below.
-  uint32_t qa[8][4];
+  uint4* qfrag = reinterpret_cast<uint4*>(smem_raw + kOffQFrag);
+  if (w == 0) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint2 hi = *reinterpret_cast<const uint2*>(qt + (g * 2) * D + 32 * t + 4 * j);
-    const uint2 lo = *reinterpret_cast<const uint2*>(qt + (g * 2 + 1) * D + 32 * t + 4 * j);
-    qa[j][0] = hi.x;
-    qa[j][1] = lo.x;
-    qa[j][2] = hi.y;
-    qa[j][3] = lo.y;
+    for (int j = 0; j < 8; ++j) {
+      const uint2 hi = *reinterpret_cast<const uint2*>(qt + (g * 2) * D + 32 * t + 4 * j);
+      const uint2 lo = *reinterpret_cast<const uint2*>(qt + (g * 2 + 1) * D + 32 * t + 4 * j);
+      qfrag[j * 32 + lane] = make_uint4(hi.x, lo.x, hi.y, lo.y);
+    }
   }
+  __syncthreads();
+  const uint32_t qfrag_addr = smem_u32(qfrag) + lane * 16;
   const float my_c = row_c[g];
   const int my_limit = row_limit[g];
   int min_limit = row_limit[0];
@@ -209,12 +215,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        uint32_t q0, q1, q2, q3;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
+                     : "r"(qfrag_addr + j * 512));
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const uint4& q4 = kw[u][j >> 2];
           const uint32_t word = (j & 3) == 0 ? q4.x : (j & 3) == 1 ? q4.y : (j & 3) == 2 ? q4.z : q4.w;
-          mma_f16(acc[u][j & 1], qa[j][0], qa[j][1], qa[j][2], qa[j][3], e4m3x2_to_f16x2(word, 0),
-                  e4m3x2_to_f16x2(word, 1));
+          mma_f16(acc[u][j & 1], q0, q1, q2, q3, e4m3x2_to_f16x2(word, 0), e4m3x2_to_f16x2(word, 1));
         }
       }
 #pragma unroll
@@ -399,7 +407,7 @@ cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(fp8fast::decode_fp8_mma_kernel, fp8fast::kSmem, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.S, a.Hkv, a.B * (a.pos_split ? a.T : 1));
+  const dim3 grid(a.S * (a.pos_split ? a.T : 1), a.Hkv, a.B);
   fp8fast::decode_fp8_mma_kernel<<<grid, fp8fast::kThreads, fp8fast::kSmem, st>>>(a);
   return cudaGetLastError();
 }

@@ -86,9 +86,12 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
   // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
   // position j of the sequence; position j attends to the first L - T + 1 + j
   // tokens (causal verify), i.e. a single-position decode over that prefix.
-  const int s = blockIdx.x, h = blockIdx.y;
-  const int b = a.pos_split ? (int)blockIdx.z / a.T : (int)blockIdx.z;
-  const int j0 = a.pos_split ? (int)blockIdx.z % a.T : 0;
+  // The T position-CTAs of one (split, head, sequence) are neighbours in
+  // launch order (x = split * T + position): they read the same pages, so the
+  // second and third reads are mostly served by L2.
+  const int s = a.pos_split ? (int)blockIdx.x / a.T : (int)blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int j0 = a.pos_split ? (int)blockIdx.x % a.T : 0;
   const int Tc = a.pos_split ? 1 : a.T;  // query positions in this CTA
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -561,7 +564,7 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel, fast::kSmem, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.S, a.Hkv, a.B * (a.pos_split ? a.T : 1));
+  const dim3 grid(a.S * (a.pos_split ? a.T : 1), a.Hkv, a.B);
   fast::decode_fp4_mma_kernel<<<grid, fast::kThreads, fast::kSmem, st>>>(a);
   return cudaGetLastError();
 }
