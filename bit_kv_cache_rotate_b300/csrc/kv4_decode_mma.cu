@@ -24,13 +24,19 @@
 // Work split: one CTA per (split, kv head, sequence); 4 consumer warps each
 // own every 4th chunk of 4 pages (64 tokens) of the split, with their own
 // online-softmax state, and merge at the end.  Each warp streams its chunks
-// with 1-D bulk copies (TMA, cp.async.bulk) into private shared-memory stages
-// completed through mbarriers, refilling a stage as soon as it is consumed.
+// with two tensor gathers (TMA cp.async.bulk.tensor tile::gather4: the 4 K and
+// the 4 V page blocks of a chunk, each block one row of a 2-D tensor map) into
+// a private shared-memory stage completed through an mbarrier, refilling the
+// stage as soon as it is consumed.
 // Four CTAs share an SM (registers capped at 128 per thread), so sixteen
 // warps' copies and math overlap; one stage per warp measured faster than
 // two stages at two CTAs per SM.  Every wait is bounded: on timeout the
 // kernel flags KV4_DEVERR_TIMEOUT and stops.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
+
+#include <mutex>
 
 #include "kv4_common.cuh"
 #include "kv4_decode.h"
@@ -48,8 +54,9 @@ constexpr int kPagesPerChunk = 4;
 constexpr int kBlk = kPage * D / 2 + kPage * D / 32;  // 1088 bytes per (page, head) block
 constexpr int kCodeBytes = kPage * D / 2;            // 1024
 constexpr int kBlkStride = 1088;                     // smem stride between staged K blocks
-constexpr int kVStride = 1104;                       // smem stride between staged V blocks (bank spread)
-constexpr int kStageBytes = kPagesPerChunk * (kBlkStride + kVStride);  // K blocks then V blocks
+constexpr int kVStride = 1088;                       // smem stride between staged V blocks (gathered rows are contiguous)
+// K blocks then V blocks; a multiple of 128 bytes (tensor copies land on 128-byte boundaries)
+constexpr int kStageBytes = (kPagesPerChunk * (kBlkStride + kVStride) + 127) / 128 * 128;
 constexpr int kStages = 1;
 // Scale tables, rows padded so the four t-lanes of a quad hit distinct banks.
 constexpr int kKTabPage = 272;                     // fp32 [8 token pairs][4 groups][2 tokens] + pad
@@ -80,7 +87,7 @@ struct Smem {
 // Rows: the R = T*G query rows of one kv head, R <= 8 (row r -> position
 // r / G, query head h*G + r % G); unused rows carry zero q and are never
 // written.
-__global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem sm{smem_raw};
   // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
@@ -152,13 +159,28 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
     const int nv = min(kPagesPerChunk, p1 - (p0 + c * kPagesPerChunk));
     uint8_t* dst = sm.stage(w, st);
     uint64_t* bar = &bars[w * kStages + st];
-    if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nv * 2 * kBlk));
-    __syncwarp();
-    if (lane < nv) {
-      const size_t blk = ((size_t)page * a.Hkv + h) * kBlk;
-      bulk_g2s(dst + lane * kBlkStride, a.k_cache + blk, kBlk, bar);
-      bulk_g2s(dst + kPagesPerChunk * kBlkStride + lane * kVStride, a.v_cache + blk, kBlk, bar);
+    // K and V: the 4 page blocks of each in one tensor gather (tile::gather4,
+    // one 1088-byte row per page block); rows past the split re-read the
+    // chunk's first block and are masked like any token past the context.
+    const int row = page * a.Hkv + h;
+    const int r0 = __shfl_sync(0xffffffffu, row, 0);
+    const int r1 = nv > 1 ? __shfl_sync(0xffffffffu, row, 1) : r0;
+    const int r2 = nv > 2 ? __shfl_sync(0xffffffffu, row, 2) : r0;
+    const int r3 = nv > 3 ? __shfl_sync(0xffffffffu, row, 3) : r0;
+    if (lane == 0) {
+      mbar_expect_tx(bar, (uint32_t)(2 * kPagesPerChunk * kBlk));
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+          "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(&kmap)), "r"(0), "r"(r0), "r"(r1),
+          "r"(r2), "r"(r3), "r"(smem_u32(bar))
+          : "memory");
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+          "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst + kPagesPerChunk * kBlkStride)), "l"(reinterpret_cast<uint64_t>(&vmap)), "r"(0), "r"(r0), "r"(r1),
+          "r"(r2), "r"(r3), "r"(smem_u32(bar))
+          : "memory");
     }
+    __syncwarp();
   };
 
   // Start streaming before the q prologue so the first loads overlap it.
@@ -564,8 +586,34 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel, fast::kSmem, smem_set);
   if (e != cudaSuccess) return e;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) return cudaErrorNotSupported;
+  // Each cache as a 2-D tensor of rows, one (page, head) block per row: 136
+  // eight-byte elements, row stride 1088 bytes.
+  CUtensorMap kmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)fast::kBlk / 8, (cuuint64_t)a.num_pages * a.Hkv};
+  const cuuint64_t strides[1] = {(cuuint64_t)fast::kBlk};
+  const cuuint32_t box[2] = {(cuuint32_t)fast::kBlk / 8, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(a.k_cache), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  CUtensorMap vmap;
+  if (encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(a.v_cache), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const dim3 grid(a.S * (a.pos_split ? a.T : 1), a.Hkv, a.B);
-  fast::decode_fp4_mma_kernel<<<grid, fast::kThreads, fast::kSmem, st>>>(a);
+  fast::decode_fp4_mma_kernel<<<grid, fast::kThreads, fast::kSmem, st>>>(a, kmap, vmap);
   return cudaGetLastError();
 }
 
