@@ -199,8 +199,7 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   } else if (!fp8 && kv4::mla_path_supported(D, G, T, latent)) {
     e = kv4::launch_decode_mla(a, st);
   } else if (!fp8 && kv4::fast_path_supported(D, G, T, latent)) {
-    a.pos_split = T * G > 8 ? 1 : 0;
-    e = kv4::launch_decode_fast(D, a, st);
+    e = kv4::launch_decode_fast(D, a, st);  // chooses row blocks or pos_split
   } else if (fp8 && kv4::fp8_fast_path_supported(D, G, T)) {
     a.pos_split = T * G > 8 ? 1 : 0;
     e = kv4::launch_decode_fp8_fast(a, st);

@@ -64,13 +64,21 @@ constexpr int kVTabPage = 160;                     // f16x2 [4 groups][8 token p
 constexpr int kKTab = kPagesPerChunk * kKTabPage;
 constexpr int kVTab = kPagesPerChunk * kVTabPage;
 constexpr int kTabBytes = kKTab + kVTab;
-constexpr int kQBytes = 8 * 2 * D * 2;             // f16 q [8 rows][hi, lo][128 ch], aliases the tables
-static_assert(kWarps * kTabBytes >= kQBytes, "q terms must fit in the table area");
-// q A-fragments, [group][k-step][lane] uint4, read per use: keeping them in
-// registers (32 per thread) spilled at the 128-register cap of four CTAs/SM.
-constexpr int kQFragOff = kWarps * kStages * kStageBytes + kWarps * kTabBytes + 8 * kWarps * kStages;
-constexpr int kSmem = kQFragOff + 4 * 2 * 32 * 16;
+constexpr int kQBytes = 8 * 2 * D * 2;             // f16 q per 8-row block [8 rows][hi, lo][128 ch]
+// The q terms (prologue only) alias the scale tables; with several row blocks
+// the shared area grows to hold them.
+__host__ __device__ constexpr int tab_area(int RB) {
+  return kWarps * kTabBytes > RB * kQBytes ? kWarps * kTabBytes : RB * kQBytes;
+}
+// q A-fragments, [row block][group][k-step][lane] uint4, read per use:
+// keeping them in registers (32 per thread per block) spilled at the
+// 128-register cap of four CTAs/SM.
+__host__ __device__ constexpr int qfrag_off(int RB) {
+  return kWarps * kStages * kStageBytes + tab_area(RB) + 8 * kWarps * kStages;
+}
+__host__ __device__ constexpr int smem_bytes(int RB) { return qfrag_off(RB) + RB * 4 * 2 * 32 * 16; }
 
+template <int RB>
 struct Smem {
   uint8_t* base;
   __device__ uint8_t* stage(int w, int s) const { return base + (w * kStages + s) * kStageBytes; }
@@ -79,17 +87,22 @@ struct Smem {
   __device__ uint32_t* vtab(int w) const { return reinterpret_cast<uint32_t*>(tabs(w) + kKTab); }
   __device__ uint8_t* qterms() const { return tabs(0); }  // prologue only
   __device__ uint64_t* bars() const {
-    return reinterpret_cast<uint64_t*>(base + kWarps * kStages * kStageBytes + kWarps * kTabBytes);
+    return reinterpret_cast<uint64_t*>(base + kWarps * kStages * kStageBytes + tab_area(RB));
   }
 };
 
 // ---------------------------------------------------------------- kernel
-// Rows: the R = T*G query rows of one kv head, R <= 8 (row r -> position
-// r / G, query head h*G + r % G); unused rows carry zero q and are never
-// written.
-__global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+// Rows: the R = T*G query rows of one kv head, R <= 8 * RB (row r -> position
+// r / G, query head h*G + r % G), in RB blocks of 8 MMA rows; unused rows
+// carry zero q and are never written.  Each K and V fragment is widened once
+// and used by every row block (a T = 3 verify step shares the decode work of
+// its three positions).
+template <int RB>
+__global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
+    decode_fp4_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                          const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem sm{smem_raw};
+  Smem<RB> sm{smem_raw};
   // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
   // position j of the sequence; position j attends to the first L - T + 1 + j
   // tokens (causal verify), i.e. a single-position decode over that prefix.
@@ -192,10 +205,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
   }
 
   // ---- q prologue: rotate (fp32 butterfly), scale row by 2^sigma, split into f16 hi + lo
-  uint16_t* qt = reinterpret_cast<uint16_t*>(sm.qterms());  // [8 rows][hi, lo][128]
-  __shared__ float row_c[8];
-  __shared__ int row_limit[8];
-  for (int r = w; r < 8; r += kWarps) {
+  uint16_t* qt = reinterpret_cast<uint16_t*>(sm.qterms());  // [8 * RB rows][hi, lo][128]
+  __shared__ float row_c[8 * RB];
+  __shared__ int row_limit[8 * RB];
+  for (int r = w; r < 8 * RB; r += kWarps) {
     float x[4];
     if (r < R) {
       const uint16_t* src = a.q + row_index(r) * D + lane * 4;
@@ -239,30 +252,43 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
   // lo.  Step j's k index 2t+i maps to channel 32G + 8t + 4j + i and 2t+8+i to
   // 32G + 8t + 4j + 2 + i, matching the K B-fragments built from one 32-bit
   // word of codes per thread (bytes 4t .. 4t+3 of the group).
-  uint4* qfrag = reinterpret_cast<uint4*>(smem_raw + kQFragOff);
-  if (w == 0) {
+  uint4* qfrag = reinterpret_cast<uint4*>(smem_raw + qfrag_off(RB));
+  for (int rb = w; rb < RB; rb += kWarps) {
+    const uint16_t* qb = qt + (8 * rb) * 2 * D;
 #pragma unroll
     for (int G4 = 0; G4 < 4; ++G4) {
-      const uint4 hi = *reinterpret_cast<const uint4*>(qt + (g * 2) * D + 32 * G4 + 8 * t);
-      const uint4 lo = *reinterpret_cast<const uint4*>(qt + (g * 2 + 1) * D + 32 * G4 + 8 * t);
-      qfrag[(G4 * 2 + 0) * 32 + lane] = make_uint4(hi.x, lo.x, hi.y, lo.y);
-      qfrag[(G4 * 2 + 1) * 32 + lane] = make_uint4(hi.z, lo.z, hi.w, lo.w);
+      const uint4 hi = *reinterpret_cast<const uint4*>(qb + (g * 2) * D + 32 * G4 + 8 * t);
+      const uint4 lo = *reinterpret_cast<const uint4*>(qb + (g * 2 + 1) * D + 32 * G4 + 8 * t);
+      qfrag[((rb * 4 + G4) * 2 + 0) * 32 + lane] = make_uint4(hi.x, lo.x, hi.y, lo.y);
+      qfrag[((rb * 4 + G4) * 2 + 1) * 32 + lane] = make_uint4(hi.z, lo.z, hi.w, lo.w);
     }
   }
   const uint32_t qfrag_addr = smem_u32(qfrag) + lane * 16;
-  const float my_c = row_c[g];
-  const int my_limit = row_limit[g];
+  float my_c[RB];
+  int my_limit[RB];
+#pragma unroll
+  for (int rb = 0; rb < RB; ++rb) {
+    my_c[rb] = row_c[8 * rb + g];
+    my_limit[rb] = row_limit[8 * rb + g];
+  }
   int min_limit = row_limit[0];
 #pragma unroll
-  for (int r = 1; r < 8; ++r) min_limit = min(min_limit, row_limit[r]);
+  for (int r = 1; r < 8 * RB; ++r) min_limit = min(min_limit, row_limit[r]);
   __syncthreads();  // the q terms share memory with the scale tables
 
   // ---- per-warp running state
-  float o[8][4];
+  float o[RB][8][4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.0f;
-  float m_run = -INFINITY;
-  float2 l2 = make_float2(0.0f, 0.0f);
+  for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[rb][j][0] = o[rb][j][1] = o[rb][j][2] = o[rb][j][3] = 0.0f;
+  float m_run[RB];
+  float2 l2[RB];
+#pragma unroll
+  for (int rb = 0; rb < RB; ++rb) {
+    m_run[rb] = -INFINITY;
+    l2[rb] = make_float2(0.0f, 0.0f);
+  }
   uint32_t eref = 0;  // 4 UE8M0 bytes: running max of V exponents per group
 
   float* ktab = sm.ktab(w);
@@ -351,17 +377,15 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
 
     // ---- Q.K^T: 8 n8 tiles, two at a time (8 independent accumulator chains);
     // tile n covers token pair n of each page (col 2t'+i -> page t', token 2n+i)
-    float2 sc[8];  // row g, tokens (2n, 2n+1) of page t
+    // n-tiles per step: two (8 independent accumulator chains) for one row
+    // block; one with several blocks, whose accumulators and O need the registers.
+    constexpr int NU = RB == 1 ? 2 : 1;
+    float2 sc[RB][8];  // row 8rb + g, tokens (2n, 2n+1) of page t
 #pragma unroll
-    for (int n = 0; n < 8; n += 2) {
-      float acc[2][4][4];
+    for (int n = 0; n < 8; n += NU) {
+      uint32_t kb[NU][4][4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4) acc[u][G4][0] = acc[u][G4][1] = acc[u][G4][2] = acc[u][G4][3] = 0.0f;
-      uint32_t kb[2][4][4];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < NU; ++u) {
         const uint8_t* krow = stg + (g >> 1) * kBlkStride + k_code_offset(D, 2 * (n + u) + (g & 1), 8 * t);
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
@@ -371,18 +395,25 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
         }
       }
 #pragma unroll
+      for (int rb = 0; rb < RB; ++rb) {
+      float acc[NU][4][4];
+#pragma unroll
+      for (int u = 0; u < NU; ++u)
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) acc[u][G4][0] = acc[u][G4][1] = acc[u][G4][2] = acc[u][G4][3] = 0.0f;
+#pragma unroll
       for (int j2 = 0; j2 < 2; ++j2)
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
           uint32_t q0, q1, q2, q3;
           asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
-                       : "r"(qfrag_addr + (G4 * 2 + j2) * 512));
+                       : "r"(qfrag_addr + ((rb * 4 + G4) * 2 + j2) * 512));
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
+          for (int u = 0; u < NU; ++u)
             mma_f16(acc[u][G4], q0, q1, q2, q3, kb[u][G4][2 * j2], kb[u][G4][2 * j2 + 1]);
         }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < NU; ++u) {
         const float4* kt =
             reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(ktab) + t * kKTabPage + (n + u) * 32);
         const float4 s01 = kt[0], s23 = kt[1];
@@ -394,67 +425,84 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
         const float2 t3 = __fadd2_rn(make_float2(ac[3][0], ac[3][1]), make_float2(ac[3][2], ac[3][3]));
         const float2 v01 = __ffma2_rn(make_float2(s01.z, s01.w), t1, __fmul2_rn(make_float2(s01.x, s01.y), t0));
         const float2 v23 = __ffma2_rn(make_float2(s23.z, s23.w), t3, __fmul2_rn(make_float2(s23.x, s23.y), t2));
-        float2 v = __fmul2_rn(__fadd2_rn(v01, v23), make_float2(my_c, my_c));
+        float2 v = __fmul2_rn(__fadd2_rn(v01, v23), make_float2(my_c[rb], my_c[rb]));
         if (edge) {
           const int posb = (pg + t) * kPage + 2 * (n + u);
           const bool ok = t < nv;
-          if (!(ok && posb < my_limit)) v.x = -INFINITY;
-          if (!(ok && posb + 1 < my_limit)) v.y = -INFINITY;
+          if (!(ok && posb < my_limit[rb])) v.x = -INFINITY;
+          if (!(ok && posb + 1 < my_limit[rb])) v.y = -INFINITY;
         }
-        sc[n + u] = v;
+        sc[rb][n + u] = v;
       }
+      }  // row blocks
     }
 
-    // ---- online softmax for row g over this chunk (the quad t = 0..3 holds the row)
-    float mx8[8];
+    // ---- online softmax per row block (row 8rb + g; the quad t = 0..3 holds the row)
+    float alpha[RB];
+    float2 p[RB][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(sc[i].x, sc[i].y);
+    for (int rb = 0; rb < RB; ++rb) {
+      float mx8[8];
 #pragma unroll
-    for (int w2 = 4; w2 >= 1; w2 >>= 1)
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(sc[rb][i].x, sc[rb][i].y);
 #pragma unroll
-      for (int i = 0; i < w2; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w2]);
-    float cmx = mx8[0];
-    cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
-    cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
-    // Lazy maximum: the row's reference moves only when the chunk maximum
-    // exceeds it by more than 8 (log2 units), so p <= 2^8 and O is rarely
-    // rescaled.  Any reference gives the same (O, l) up to that common factor.
-    const float m_new = cmx > m_run + 8.0f ? cmx : m_run;
-    float alpha = 1.0f;
-    float2 p[8];
-    if (m_new == -INFINITY) {
+      for (int w2 = 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) p[i] = make_float2(0.0f, 0.0f);
-    } else {
-      alpha = ex2(m_run - m_new);
-      const float2 nm = make_float2(-m_new, -m_new);
+        for (int i = 0; i < w2; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w2]);
+      float cmx = mx8[0];
+      cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
+      cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
+      // Lazy maximum: the row's reference moves only when the chunk maximum
+      // exceeds it by more than 8 (log2 units), so p <= 2^8 and O is rarely
+      // rescaled.  Any reference gives the same (O, l) up to that common factor.
+      const float m_new = cmx > m_run[rb] + 8.0f ? cmx : m_run[rb];
+      alpha[rb] = 1.0f;
+      if (m_new == -INFINITY) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float2 d2 = __fadd2_rn(sc[i], nm);
-        p[i] = make_float2(ex2(d2.x), ex2(d2.y));
+        for (int i = 0; i < 8; ++i) p[rb][i] = make_float2(0.0f, 0.0f);
+      } else {
+        alpha[rb] = ex2(m_run[rb] - m_new);
+        const float2 nm = make_float2(-m_new, -m_new);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 d2 = __fadd2_rn(sc[rb][i], nm);
+          p[rb][i] = make_float2(ex2(d2.x), ex2(d2.y));
+        }
+        const float2 ls =
+            __fadd2_rn(__fadd2_rn(__fadd2_rn(p[rb][0], p[rb][1]), __fadd2_rn(p[rb][2], p[rb][3])),
+                       __fadd2_rn(__fadd2_rn(p[rb][4], p[rb][5]), __fadd2_rn(p[rb][6], p[rb][7])));
+        l2[rb] = __ffma2_rn(l2[rb], make_float2(alpha[rb], alpha[rb]), ls);
       }
-      const float2 ls = __fadd2_rn(__fadd2_rn(__fadd2_rn(p[0], p[1]), __fadd2_rn(p[2], p[3])),
-                                   __fadd2_rn(__fadd2_rn(p[4], p[5]), __fadd2_rn(p[6], p[7])));
-      l2 = __ffma2_rn(l2, make_float2(alpha, alpha), ls);
+      m_run[rb] = m_new;
     }
-    m_run = m_new;
 
-    // ---- rescale O: columns 2t, 2t+1 are query rows 2t, 2t+1; group factor 2^(Eold - Enew)
-    const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * t);
-    const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-    if (__any_sync(0xffffffffu, eold != eref || a0 != 1.0f || a1 != 1.0f)) {
-      const uint32_t dl = __vsubus4(eref, eold);  // Enew - Eold per group
+    // ---- rescale O: columns 2t, 2t+1 are rows 8rb + 2t, 8rb + 2t + 1; group factor 2^(Eold - Enew)
+    {
+      float a0[RB], a1[RB];
+      bool any_a = false;
 #pragma unroll
-      for (int G4 = 0; G4 < 4; ++G4) {
-        const int ex = 127 - (int)((dl >> (8 * G4)) & 0xFFu);
-        const float f = ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f;
-        const float f0 = f * a0, f1 = f * a1;
+      for (int rb = 0; rb < RB; ++rb) {
+        a0[rb] = __shfl_sync(0xffffffffu, alpha[rb], 8 * t);
+        a1[rb] = __shfl_sync(0xffffffffu, alpha[rb], 8 * t + 4);
+        any_a |= a0[rb] != 1.0f || a1[rb] != 1.0f;
+      }
+      if (__any_sync(0xffffffffu, eold != eref || any_a)) {
+        const uint32_t dl = __vsubus4(eref, eold);  // Enew - Eold per group
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          o[2 * G4 + jj][0] *= f0;
-          o[2 * G4 + jj][1] *= f1;
-          o[2 * G4 + jj][2] *= f0;
-          o[2 * G4 + jj][3] *= f1;
+        for (int G4 = 0; G4 < 4; ++G4) {
+          const int ex = 127 - (int)((dl >> (8 * G4)) & 0xFFu);
+          const float f = ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f;
+#pragma unroll
+          for (int rb = 0; rb < RB; ++rb) {
+            const float f0 = f * a0[rb], f1 = f * a1[rb];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              o[rb][2 * G4 + jj][0] *= f0;
+              o[rb][2 * G4 + jj][1] *= f1;
+              o[rb][2 * G4 + jj][2] *= f0;
+              o[rb][2 * G4 + jj][3] *= f1;
+            }
+          }
         }
       }
     }
@@ -463,18 +511,22 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
     // The lo part matters only for large p: its MMAs run for a k-step only when
     // some p of the step (any row, any page) exceeds 2^-8; below that the f16
     // rounding of p alone stays under 2^-20 per token.
-    uint32_t ph[4][2], pl[4][2];
+    uint32_t ph[RB][4][2], pl[RB][4][2];
     bool need_lo[4];
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
-      float2 h0, l0, h1, l1;
-      split_hi_lo2(p[2 * c4], h0, l0);
-      split_hi_lo2(p[2 * c4 + 1], h1, l1);
-      ph[c4][0] = pack_f16x2(h0.x, h0.y);
-      ph[c4][1] = pack_f16x2(h1.x, h1.y);
-      pl[c4][0] = pack_f16x2(l0.x, l0.y);
-      pl[c4][1] = pack_f16x2(l1.x, l1.y);
-      const float pm = fmaxf(fmaxf(p[2 * c4].x, p[2 * c4].y), fmaxf(p[2 * c4 + 1].x, p[2 * c4 + 1].y));
+      float pm = 0.0f;
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb) {
+        float2 h0, l0, h1, l1;
+        split_hi_lo2(p[rb][2 * c4], h0, l0);
+        split_hi_lo2(p[rb][2 * c4 + 1], h1, l1);
+        ph[rb][c4][0] = pack_f16x2(h0.x, h0.y);
+        ph[rb][c4][1] = pack_f16x2(h1.x, h1.y);
+        pl[rb][c4][0] = pack_f16x2(l0.x, l0.y);
+        pl[rb][c4][1] = pack_f16x2(l1.x, l1.y);
+        pm = fmaxf(pm, fmaxf(fmaxf(p[rb][2 * c4].x, p[rb][2 * c4].y), fmaxf(p[rb][2 * c4 + 1].x, p[rb][2 * c4 + 1].y)));
+      }
       need_lo[c4] = __any_sync(0xffffffffu, pm > 0.00390625f);
     }
 
@@ -495,19 +547,22 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
-        const uint32_t ph0 = hmul2(ph[c4][0], vsc[2 * c4]), ph1 = hmul2(ph[c4][1], vsc[2 * c4 + 1]);
         const uint32_t wA0 = c4 < 2 ? rA0.x : rA0.y, wB0 = c4 < 2 ? rB0.x : rB0.y;
         const uint32_t wA1 = c4 < 2 ? rA1.x : rA1.y, wB1 = c4 < 2 ? rB1.x : rB1.y;
         const uint32_t x00 = e2m1x2_to_f16x2(wA0, b0), x01 = e2m1x2_to_f16x2(wB0, b0);
         const uint32_t x02 = e2m1x2_to_f16x2(wA0, b1), x03 = e2m1x2_to_f16x2(wB0, b1);
         const uint32_t x10 = e2m1x2_to_f16x2(wA1, b0), x11 = e2m1x2_to_f16x2(wB1, b0);
         const uint32_t x12 = e2m1x2_to_f16x2(wA1, b1), x13 = e2m1x2_to_f16x2(wB1, b1);
-        mma_f16(o[2 * G4], x00, x01, x02, x03, ph0, ph1);
-        mma_f16(o[2 * G4 + 1], x10, x11, x12, x13, ph0, ph1);
-        if (need_lo[c4]) {
-          const uint32_t pl0 = hmul2(pl[c4][0], vsc[2 * c4]), pl1 = hmul2(pl[c4][1], vsc[2 * c4 + 1]);
-          mma_f16(o[2 * G4], x00, x01, x02, x03, pl0, pl1);
-          mma_f16(o[2 * G4 + 1], x10, x11, x12, x13, pl0, pl1);
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb) {
+          const uint32_t ph0 = hmul2(ph[rb][c4][0], vsc[2 * c4]), ph1 = hmul2(ph[rb][c4][1], vsc[2 * c4 + 1]);
+          mma_f16(o[rb][2 * G4], x00, x01, x02, x03, ph0, ph1);
+          mma_f16(o[rb][2 * G4 + 1], x10, x11, x12, x13, ph0, ph1);
+          if (need_lo[c4]) {
+            const uint32_t pl0 = hmul2(pl[rb][c4][0], vsc[2 * c4]), pl1 = hmul2(pl[rb][c4][1], vsc[2 * c4 + 1]);
+            mma_f16(o[rb][2 * G4], x00, x01, x02, x03, pl0, pl1);
+            mma_f16(o[rb][2 * G4 + 1], x10, x11, x12, x13, pl0, pl1);
+          }
         }
       }
     }
@@ -529,63 +584,82 @@ __global__ void __launch_bounds__(kThreads, 4) decode_fp4_mma_kernel(DecodeArgs 
         (void)mbar_wait(&bars[w * kStages + it % kStages], (uint32_t)((it / kStages) & 1));
   }
 
-  // ---- merge the 4 warps: row l sums, then O scaled by 2^Eref_G and exp2(m_w - M)
-  float l_row = l2.x + l2.y;
-  l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
-  l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
-  __syncthreads();  // all warps done with their stages: reuse smem for the merge
+  // ---- merge the 4 warps, one row block at a time: row l sums, then O scaled
+  // by 2^Eref_G and exp2(m_w - M)
   float* mo = reinterpret_cast<float*>(smem_raw);  // [kWarps][8 rows][D]
   float* mm = mo + kWarps * 8 * D;                  // [kWarps][8]
   float* ml = mm + kWarps * 8;                      // [kWarps][8]
-  if (t == 0) {
-    mm[w * 8 + g] = m_run;
-    ml[w * 8 + g] = l_row;
-  }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float eg = __uint_as_float(((eref >> (8 * (j >> 1))) & 0xFFu) << 23);
-    mo[(w * 8 + 2 * t) * D + 16 * j + g] = o[j][0] * eg;
-    mo[(w * 8 + 2 * t + 1) * D + 16 * j + g] = o[j][1] * eg;
-    mo[(w * 8 + 2 * t) * D + 16 * j + g + 8] = o[j][2] * eg;
-    mo[(w * 8 + 2 * t + 1) * D + 16 * j + g + 8] = o[j][3] * eg;
-  }
-  __syncthreads();
-  // warp w finalises rows w and w+4
-  for (int r = w; r < 8; r += kWarps) {
-    if (r >= R) continue;
-    float M = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mm[ww * 8 + r]);
-    float wsum = 0.0f, wt[kWarps];
-#pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) {
-      wt[ww] = (M == -INFINITY || mm[ww * 8 + r] == -INFINITY) ? 0.0f : exp2f(mm[ww * 8 + r] - M);
-      wsum += wt[ww] * ml[ww * 8 + r];
+  for (int rb = 0; rb < RB; ++rb) {
+    float l_row = l2[rb].x + l2[rb].y;
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 1);
+    l_row += __shfl_xor_sync(0xffffffffu, l_row, 2);
+    __syncthreads();  // stages (first block) or the previous block's merge are done with
+    if (t == 0) {
+      mm[w * 8 + g] = m_run[rb];
+      ml[w * 8 + g] = l_row;
     }
-    const size_t rr = row_index(r) * a.S + s;
-    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-    for (int d = lane; d < D; d += 32) {
-      float acc = 0.0f;
 #pragma unroll
-      for (int ww = 0; ww < kWarps; ++ww) acc = fmaf(wt[ww], mo[(ww * 8 + r) * D + d], acc);
-      a.part_o[rr * D + d] = acc * inv;
+    for (int j = 0; j < 8; ++j) {
+      const float eg = __uint_as_float(((eref >> (8 * (j >> 1))) & 0xFFu) << 23);
+      mo[(w * 8 + 2 * t) * D + 16 * j + g] = o[rb][j][0] * eg;
+      mo[(w * 8 + 2 * t + 1) * D + 16 * j + g] = o[rb][j][1] * eg;
+      mo[(w * 8 + 2 * t) * D + 16 * j + g + 8] = o[rb][j][2] * eg;
+      mo[(w * 8 + 2 * t + 1) * D + 16 * j + g + 8] = o[rb][j][3] * eg;
     }
-    if (lane == 0) a.part_lse[rr] = wsum > 0.0f ? (M + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+    __syncthreads();
+    // warp w finalises rows w and w+4 of the block
+    for (int r = w; r < 8; r += kWarps) {
+      const int rr_row = 8 * rb + r;
+      if (rr_row >= R) continue;
+      float M = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mm[ww * 8 + r]);
+      float wsum = 0.0f, wt[kWarps];
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) {
+        wt[ww] = (M == -INFINITY || mm[ww * 8 + r] == -INFINITY) ? 0.0f : exp2f(mm[ww * 8 + r] - M);
+        wsum += wt[ww] * ml[ww * 8 + r];
+      }
+      const size_t rr = row_index(rr_row) * a.S + s;
+      const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+      for (int d = lane; d < D; d += 32) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) acc = fmaf(wt[ww], mo[(ww * 8 + r) * D + d], acc);
+        a.part_o[rr * D + d] = acc * inv;
+      }
+      if (lane == 0) a.part_lse[rr] = wsum > 0.0f ? (M + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+    }
   }
 }
 
 }  // namespace fast
 
 bool fast_path_supported(int D, int G, int T, bool latent) {
-  (void)T;  // T * G > 8 runs one CTA per query position (pos_split)
+  (void)T;  // more than 24 rows run one CTA per query position (pos_split)
   return D == 128 && !latent && G <= 8;
 }
 
-cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
-  if (D != 128) return cudaErrorNotSupported;
+namespace {
+
+template <int RB>
+cudaError_t launch_rb(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
-  const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel, fast::kSmem, smem_set);
+  const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel<RB>, fast::smem_bytes(RB), smem_set);
   if (e != cudaSuccess) return e;
+  const dim3 grid(a.S * (a.pos_split ? a.T : 1), a.Hkv, a.B);
+  fast::decode_fp4_mma_kernel<RB><<<grid, fast::kThreads, fast::smem_bytes(RB), st>>>(a, kmap, vmap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Up to 24 query rows per kv head (T * G <= 24, e.g. a T = 3 verify step with
+// G = 8) run in one CTA as 1-3 row blocks; more rows run one CTA per query
+// position (pos_split).
+cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st) {
+  if (D != 128) return cudaErrorNotSupported;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -598,23 +672,23 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st) {
   if (!encode) return cudaErrorNotSupported;
   // Each cache as a 2-D tensor of rows, one (page, head) block per row: 136
   // eight-byte elements, row stride 1088 bytes.
-  CUtensorMap kmap;
-  const cuuint64_t dims[2] = {(cuuint64_t)fast::kBlk / 8, (cuuint64_t)a.num_pages * a.Hkv};
+  CUtensorMap kmap, vmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)fast::kBlk / 8, (cuuint64_t)a_in.num_pages * a_in.Hkv};
   const cuuint64_t strides[1] = {(cuuint64_t)fast::kBlk};
   const cuuint32_t box[2] = {(cuuint32_t)fast::kBlk / 8, 1};
   const cuuint32_t estr[2] = {1, 1};
-  if (encode(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(a.k_cache), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  CUtensorMap vmap;
-  if (encode(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(a.v_cache), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  const dim3 grid(a.S * (a.pos_split ? a.T : 1), a.Hkv, a.B);
-  fast::decode_fp4_mma_kernel<<<grid, fast::kThreads, fast::kSmem, st>>>(a, kmap, vmap);
-  return cudaGetLastError();
+  for (int i = 0; i < 2; ++i) {
+    if (encode(i ? &vmap : &kmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
+               const_cast<uint8_t*>(i ? a_in.v_cache : a_in.k_cache), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  DecodeArgs a = a_in;
+  const int R = a.T * (a.Hq / a.Hkv);
+  a.pos_split = R > 24 ? 1 : 0;
+  if (a.pos_split || R <= 8) return launch_rb<1>(a, kmap, vmap, st);
+  return R <= 16 ? launch_rb<2>(a, kmap, vmap, st) : launch_rb<3>(a, kmap, vmap, st);
 }
 
 }  // namespace kv4
