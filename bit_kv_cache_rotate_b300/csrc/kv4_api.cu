@@ -149,6 +149,9 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   if (!q || !k_cache || !block_tables || !context_lens || !workspace || (combine && !out))
     return KV4_ERR_INVALID_ARG;
   if (!combine && num_splits < 1) return KV4_ERR_INVALID_ARG;
+  // The kernels take the softmax maximum over unscaled logits; a positive,
+  // finite factor keeps that maximum the maximum of the scaled ones.
+  if (!(softmax_scale > 0.0f) || !isfinite(softmax_scale)) return KV4_ERR_INVALID_ARG;
   if (fp8 && (!v_cache || !k_scale || !v_scale)) return KV4_ERR_INVALID_ARG;
   if (((uintptr_t)q & 15) || ((uintptr_t)k_cache & 15) || ((uintptr_t)v_cache & 15) ||
       ((uintptr_t)workspace & 255) || (combine && ((uintptr_t)out & 15)))

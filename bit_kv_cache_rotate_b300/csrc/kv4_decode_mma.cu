@@ -18,8 +18,8 @@
 //           are widened the same way; the V scale enters as 2^(e_v - Eref_G)
 //           multiplied into the P fragments of group G, Eref_G being a per-
 //           warp reference exponent (O rows of the group are rescaled when it
-//           rises).  P is split into f16 hi + lo parts (Veltkamp), so P.V
-//           carries about 22 bits of P.
+//           rises).  P is split into f16 hi + lo parts (p rounded to f16
+//           and the rounded remainder), so P.V carries about 22 bits of P.
 //
 // Work split: one CTA per (split, kv head, sequence); 4 consumer warps each
 // own every 4th chunk of 4 pages (64 tokens) of the split, with their own
@@ -375,66 +375,60 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
       __syncwarp();
     }
 
-    // ---- Q.K^T: 8 n8 tiles, two at a time (8 independent accumulator chains);
-    // tile n covers token pair n of each page (col 2t'+i -> page t', token 2n+i)
-    // n-tiles per step: two (8 independent accumulator chains) for one row
-    // block; one with several blocks, whose accumulators and O need the registers.
-    constexpr int NU = RB == 1 ? 2 : 1;
+    // ---- Q.K^T, group-major: per 32-channel group G the q fragments are read
+    // once for NB n-tiles (tile n: token pair n of each page, col 2t'+i -> page
+    // t', token 2n+i); each tile's group result (hi row + lo row) is multiplied
+    // by that group's K scale and accumulated over the groups.  The row factor
+    // (softmax scale, log2 e, 2^-sigma) is applied in the softmax below.
+    constexpr int NB = RB == 1 ? 4 : 2;
     float2 sc[RB][8];  // row 8rb + g, tokens (2n, 2n+1) of page t
+    const uint8_t* ktb = reinterpret_cast<const uint8_t*>(ktab) + t * kKTabPage;
 #pragma unroll
-    for (int n = 0; n < 8; n += NU) {
-      uint32_t kb[NU][4][4];
+    for (int n0 = 0; n0 < 8; n0 += NB) {
 #pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        const uint8_t* krow = stg + (g >> 1) * kBlkStride + k_code_offset(D, 2 * (n + u) + (g & 1), 8 * t);
+      for (int G4 = 0; G4 < 4; ++G4) {
+        uint32_t kb[NB][4];
 #pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4) {
-          const uint32_t x = *reinterpret_cast<const uint32_t*>(krow + 128 * G4);
+        for (int u = 0; u < NB; ++u) {
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(
+              stg + (g >> 1) * kBlkStride + k_code_offset(D, 2 * (n0 + u) + (g & 1), 8 * t) + 128 * G4);
 #pragma unroll
-          for (int bb = 0; bb < 4; ++bb) kb[u][G4][bb] = e2m1x2_to_f16x2(x, bb);
+          for (int bb = 0; bb < 4; ++bb) kb[u][bb] = e2m1x2_to_f16x2(x, bb);
+        }
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb) {
+          float acc[NB][4];
+#pragma unroll
+          for (int u = 0; u < NB; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
+#pragma unroll
+          for (int j2 = 0; j2 < 2; ++j2) {
+            uint32_t q0, q1, q2, q3;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
+                         : "r"(qfrag_addr + ((rb * 4 + G4) * 2 + j2) * 512));
+#pragma unroll
+            for (int u = 0; u < NB; ++u) mma_f16(acc[u], q0, q1, q2, q3, kb[u][2 * j2], kb[u][2 * j2 + 1]);
+          }
+#pragma unroll
+          for (int u = 0; u < NB; ++u) {
+            const float2 ks = *reinterpret_cast<const float2*>(ktb + (n0 + u) * 32 + G4 * 8);
+            const float2 tt = __fadd2_rn(make_float2(acc[u][0], acc[u][1]), make_float2(acc[u][2], acc[u][3]));
+            sc[rb][n0 + u] = G4 == 0 ? __fmul2_rn(ks, tt) : __ffma2_rn(ks, tt, sc[rb][n0 + u]);
+          }
         }
       }
+    }
+
+    // tokens past the split's pages, the context or a row's causal limit
+    if (edge) {
 #pragma unroll
-      for (int rb = 0; rb < RB; ++rb) {
-      float acc[NU][4][4];
+      for (int rb = 0; rb < RB; ++rb)
 #pragma unroll
-      for (int u = 0; u < NU; ++u)
-#pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4) acc[u][G4][0] = acc[u][G4][1] = acc[u][G4][2] = acc[u][G4][3] = 0.0f;
-#pragma unroll
-      for (int j2 = 0; j2 < 2; ++j2)
-#pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4) {
-          uint32_t q0, q1, q2, q3;
-          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
-                       : "r"(qfrag_addr + ((rb * 4 + G4) * 2 + j2) * 512));
-#pragma unroll
-          for (int u = 0; u < NU; ++u)
-            mma_f16(acc[u][G4], q0, q1, q2, q3, kb[u][G4][2 * j2], kb[u][G4][2 * j2 + 1]);
-        }
-#pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        const float4* kt =
-            reinterpret_cast<const float4*>(reinterpret_cast<const uint8_t*>(ktab) + t * kKTabPage + (n + u) * 32);
-        const float4 s01 = kt[0], s23 = kt[1];
-        float (&ac)[4][4] = acc[u];
-        // rows g (hi) + g+8 (lo) of each group, then the groups' K scales
-        const float2 t0 = __fadd2_rn(make_float2(ac[0][0], ac[0][1]), make_float2(ac[0][2], ac[0][3]));
-        const float2 t1 = __fadd2_rn(make_float2(ac[1][0], ac[1][1]), make_float2(ac[1][2], ac[1][3]));
-        const float2 t2 = __fadd2_rn(make_float2(ac[2][0], ac[2][1]), make_float2(ac[2][2], ac[2][3]));
-        const float2 t3 = __fadd2_rn(make_float2(ac[3][0], ac[3][1]), make_float2(ac[3][2], ac[3][3]));
-        const float2 v01 = __ffma2_rn(make_float2(s01.z, s01.w), t1, __fmul2_rn(make_float2(s01.x, s01.y), t0));
-        const float2 v23 = __ffma2_rn(make_float2(s23.z, s23.w), t3, __fmul2_rn(make_float2(s23.x, s23.y), t2));
-        float2 v = __fmul2_rn(__fadd2_rn(v01, v23), make_float2(my_c[rb], my_c[rb]));
-        if (edge) {
-          const int posb = (pg + t) * kPage + 2 * (n + u);
+        for (int n = 0; n < 8; ++n) {
+          const int posb = (pg + t) * kPage + 2 * n;
           const bool ok = t < nv;
-          if (!(ok && posb < my_limit[rb])) v.x = -INFINITY;
-          if (!(ok && posb + 1 < my_limit[rb])) v.y = -INFINITY;
+          if (!(ok && posb < my_limit[rb])) sc[rb][n].x = -INFINITY;
+          if (!(ok && posb + 1 < my_limit[rb])) sc[rb][n].y = -INFINITY;
         }
-        sc[rb][n + u] = v;
-      }
-      }  // row blocks
     }
 
     // ---- online softmax per row block (row 8rb + g; the quad t = 0..3 holds the row)
@@ -452,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
       float cmx = mx8[0];
       cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 1));
       cmx = fmaxf(cmx, __shfl_xor_sync(0xffffffffu, cmx, 2));
+      // to log2 units: the row factor is positive (the softmax scale is checked
+      // at the API), so the maximum of the scaled logits is the scaled maximum
+      cmx *= my_c[rb];
       // Lazy maximum: the row's reference moves only when the chunk maximum
       // exceeds it by more than 8 (log2 units), so p <= 2^8 and O is rarely
       // rescaled.  Any reference gives the same (O, l) up to that common factor.
@@ -465,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
         const float2 nm = make_float2(-m_new, -m_new);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 d2 = __fadd2_rn(sc[rb][i], nm);
+          const float2 d2 = __ffma2_rn(sc[rb][i], make_float2(my_c[rb], my_c[rb]), nm);
           p[rb][i] = make_float2(ex2(d2.x), ex2(d2.y));
         }
         const float2 ls =
@@ -508,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     }
 
     // ---- P fragments (hi + lo f16): k-step c4 uses tokens 4c4..4c4+3 of page t.
+    // hi is p rounded to f16, lo the exact fp32 remainder p - hi rounded to f16.
     // The lo part matters only for large p: its MMAs run for a k-step only when
     // some p of the step (any row, any page) exceeds 2^-8; below that the f16
     // rounding of p alone stays under 2^-20 per token.
@@ -518,11 +516,12 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
       float pm = 0.0f;
 #pragma unroll
       for (int rb = 0; rb < RB; ++rb) {
-        float2 h0, l0, h1, l1;
-        split_hi_lo2(p[rb][2 * c4], h0, l0);
-        split_hi_lo2(p[rb][2 * c4 + 1], h1, l1);
-        ph[rb][c4][0] = pack_f16x2(h0.x, h0.y);
-        ph[rb][c4][1] = pack_f16x2(h1.x, h1.y);
+        ph[rb][c4][0] = pack_f16x2(p[rb][2 * c4].x, p[rb][2 * c4].y);
+        ph[rb][c4][1] = pack_f16x2(p[rb][2 * c4 + 1].x, p[rb][2 * c4 + 1].y);
+        const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&ph[rb][c4][0]));
+        const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&ph[rb][c4][1]));
+        const float2 l0 = __fadd2_rn(p[rb][2 * c4], make_float2(-h0.x, -h0.y));
+        const float2 l1 = __fadd2_rn(p[rb][2 * c4 + 1], make_float2(-h1.x, -h1.y));
         pl[rb][c4][0] = pack_f16x2(l0.x, l0.y);
         pl[rb][c4][1] = pack_f16x2(l1.x, l1.y);
         pm = fmaxf(pm, fmaxf(fmaxf(p[rb][2 * c4].x, p[rb][2 * c4].y), fmaxf(p[rb][2 * c4 + 1].x, p[rb][2 * c4 + 1].y)));

@@ -123,7 +123,8 @@ size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int
  *   context_lens  device int32 [batch]: tokens in the cache for each sequence,
  *                 counting the q_per_seq new ones.  Query position j attends
  *                 to tokens t < context_lens[b] - q_per_seq + 1 + j.
- *   softmax_scale multiplies q.k before the softmax.
+ *   softmax_scale multiplies q.k before the softmax; finite and > 0, else
+ *                 KV4_ERR_INVALID_ARG.
  *   num_splits    KV splits per sequence (0 = kv4_decode_auto_splits).
  *   workspace     device, >= kv4_decode_workspace_bytes(...) bytes.
  *   out           device fp32 [batch][q_per_seq][num_q_heads][head_dim],

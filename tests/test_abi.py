@@ -79,6 +79,10 @@ def test_host_validation_rejects_before_launch(lib):
     assert dec(*args(ws=16)) == kv4.KV4_ERR_INVALID_ARG
     assert dec(*args(q=None)) == kv4.KV4_ERR_INVALID_ARG
     assert dec(*args(B=0)) == kv4.KV4_OK
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        a_bad = args()
+        a_bad[13] = bad
+        assert dec(*a_bad) == kv4.KV4_ERR_INVALID_ARG, bad
     assert lib.kv4_split_combine(None, None, 1, 1, 8, 128, 2, None, None) == kv4.KV4_ERR_INVALID_ARG
     assert lib.kv4_split_combine(fake, fake, 1, 1, 8, 100, 2, fake, None) == kv4.KV4_ERR_UNSUPPORTED
 
