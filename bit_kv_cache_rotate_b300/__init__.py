@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(_PKG, "libkv4.so")
 
 KV4_OK, KV4_ERR_INVALID_ARG, KV4_ERR_UNSUPPORTED, KV4_ERR_CUDA, KV4_ERR_DEVICE_BOUNDS = range(5)
 KV4_DEVERR_PAGE, KV4_DEVERR_CONTEXT, KV4_DEVERR_SLOT = 1, 2, 4
+KV4_MAX_Q_PER_SEQ = 4096  # include/kv4.h
 PAGE_SIZE = 16
 
 EXPORTS = ("kv4_status_string", "kv4_cache_bytes", "kv4_append_quantize", "kv4_decode_auto_splits",

@@ -50,7 +50,7 @@ kv4_status check_decode_shape(int batch, int T, int Hq, int Hkv, int D, int P, i
   if (batch < 0 || T < 1 || Hq < 1 || Hkv < 1 || max_pages < 1 || num_pages < 1)
     return KV4_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return KV4_ERR_INVALID_ARG;
-  if (!valid_dim(D) || P != kv4::kPage || T > 8) return KV4_ERR_UNSUPPORTED;
+  if (!valid_dim(D) || P != kv4::kPage || T > KV4_MAX_Q_PER_SEQ) return KV4_ERR_UNSUPPORTED;
   return KV4_OK;
 }
 
@@ -119,11 +119,13 @@ kv4_status fp8_append_quantize(const void* k, const void* v, int num_tokens, int
 
 int kv4_decode_auto_splits(int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
                            int head_dim, int page_size, int max_pages_per_seq) {
-  (void)q_per_seq;
-  (void)num_q_heads;
   (void)page_size;
-  if (batch < 1 || num_kv_heads < 1 || max_pages_per_seq < 1) return 1;
-  return kv4::choose_splits(batch * num_kv_heads, max_pages_per_seq, head_dim, sm_count());
+  if (batch < 1 || num_kv_heads < 1 || max_pages_per_seq < 1 || q_per_seq < 1 || num_q_heads < 1) return 1;
+  // CTAs per split: one per (sequence, kv head) and position tile
+  const long long rows = (long long)q_per_seq * (num_q_heads / num_kv_heads > 0 ? num_q_heads / num_kv_heads : 1);
+  const long long tiles = rows > kv4::kTileRows ? (rows + kv4::kTileRows - 1) / kv4::kTileRows : 1;
+  const long long units = (long long)batch * num_kv_heads * tiles;
+  return kv4::choose_splits(units > (1 << 30) ? (1 << 30) : (int)units, max_pages_per_seq, head_dim, sm_count());
 }
 
 size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int head_dim,
@@ -197,6 +199,7 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   const char* tc_env = getenv("KV4_DECODE_TCGEN05");
   const bool use_tc = tc_env != nullptr && tc_env[0] == '1';
   a.pos_split = 0;
+  a.pos_tile = 1;
   if (!fp8 && use_tc && kv4::tc_path_supported(D, G, T, latent)) {
     e = kv4::launch_decode_tc(a, st);
   } else if (!fp8 && kv4::mla_path_supported(D, G, T, latent)) {

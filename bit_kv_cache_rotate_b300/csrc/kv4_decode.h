@@ -20,7 +20,8 @@ struct DecodeArgs {
   int32_t* dev_error;
   int B, T, Hq, Hkv, max_pages, num_pages, S;
   int latent;
-  int pos_split;           // 1: one CTA per query position (grid x = S * T)
+  int pos_split;           // 1: query positions split over CTAs, pos_tile per CTA
+  int pos_tile;            //    (grid x = S * ceil(T / pos_tile), split-major)
   float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
 };
 
@@ -30,6 +31,10 @@ struct DecodeArgs {
 // four pages per split.
 // The latent (head_dim 512) kernel is compute-bound at two CTAs per SM:
 // about one wave, so the split partials stay small.
+// Query rows per CTA above which the positions are tiled over CTAs (the
+// warp-MMA kernel's three 8-row blocks).
+constexpr int kTileRows = 24;
+
 inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
   const int target = head_dim == 512 ? 2 * sms : 7 * sms;
   int s = (target + units / 2) / units;

@@ -45,16 +45,18 @@ static_assert(kWarps * kStageBytes >= kWarps * 8 * D * 4 + 2 * kWarps * 8 * 4, "
 
 __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
-  // position j of the sequence; position j attends to the first L - T + 1 + j
-  // tokens (causal verify), i.e. a single-position decode over that prefix.
-  // The T position-CTAs of one (split, head, sequence) are neighbours in
-  // launch order (x = split * T + position): they read the same pages, so the
-  // second and third reads are mostly served by L2.
-  const int s = a.pos_split ? (int)blockIdx.x / a.T : (int)blockIdx.x;
+  // With pos_split (more query rows than one CTA holds) a CTA serves the
+  // pos_tile query positions j0 .. j0 + Tc - 1 of the sequence; position j
+  // attends to the first L - T + 1 + j tokens (causal verify or extend), so
+  // the tile is a decode of Tc positions over the prefix its last position
+  // sees.  The tiles of one (split, head, sequence) are neighbours in launch
+  // order (x = split * tiles + tile): they read the same pages, so all but
+  // the first read are mostly served by L2.
+  const int n_tiles = a.pos_split ? (a.T + a.pos_tile - 1) / a.pos_tile : 1;
+  const int s = (int)blockIdx.x / n_tiles;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int j0 = a.pos_split ? (int)blockIdx.x % a.T : 0;
-  const int Tc = a.pos_split ? 1 : a.T;  // query positions in this CTA
+  const int j0 = a.pos_split ? ((int)blockIdx.x % n_tiles) * a.pos_tile : 0;
+  const int Tc = a.pos_split ? min(a.pos_tile, a.T - j0) : a.T;  // query positions in this CTA
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int G = a.Hq / a.Hkv;
@@ -407,7 +409,7 @@ cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(fp8fast::decode_fp8_mma_kernel, fp8fast::kSmem, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.S * (a.pos_split ? a.T : 1), a.Hkv, a.B);
+  const dim3 grid(a.S * (a.pos_split ? (a.T + a.pos_tile - 1) / a.pos_tile : 1), a.Hkv, a.B);
   fp8fast::decode_fp8_mma_kernel<<<grid, fp8fast::kThreads, fp8fast::kSmem, st>>>(a);
   return cudaGetLastError();
 }

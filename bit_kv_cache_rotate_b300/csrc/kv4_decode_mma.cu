@@ -103,16 +103,18 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
                           const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<RB> sm{smem_raw};
-  // With pos_split (T*G above the 8 MMA rows) a CTA serves one query
-  // position j of the sequence; position j attends to the first L - T + 1 + j
-  // tokens (causal verify), i.e. a single-position decode over that prefix.
-  // The T position-CTAs of one (split, head, sequence) are neighbours in
-  // launch order (x = split * T + position): they read the same pages, so the
-  // second and third reads are mostly served by L2.
-  const int s = a.pos_split ? (int)blockIdx.x / a.T : (int)blockIdx.x;
+  // With pos_split (more query rows than one CTA holds) a CTA serves the
+  // pos_tile query positions j0 .. j0 + Tc - 1 of the sequence; position j
+  // attends to the first L - T + 1 + j tokens (causal verify or extend), so
+  // the tile is a decode of Tc positions over the prefix its last position
+  // sees.  The tiles of one (split, head, sequence) are neighbours in launch
+  // order (x = split * tiles + tile): they read the same pages, so all but
+  // the first read are mostly served by L2.
+  const int n_tiles = a.pos_split ? (a.T + a.pos_tile - 1) / a.pos_tile : 1;
+  const int s = (int)blockIdx.x / n_tiles;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int j0 = a.pos_split ? (int)blockIdx.x % a.T : 0;
-  const int Tc = a.pos_split ? 1 : a.T;  // query positions in this CTA
+  const int j0 = a.pos_split ? ((int)blockIdx.x % n_tiles) * a.pos_tile : 0;
+  const int Tc = a.pos_split ? min(a.pos_tile, a.T - j0) : a.T;  // query positions in this CTA
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int G = a.Hq / a.Hkv;
@@ -636,18 +638,21 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
 }  // namespace fast
 
 bool fast_path_supported(int D, int G, int T, bool latent) {
-  (void)T;  // more than 24 rows run one CTA per query position (pos_split)
+  (void)T;  // more than 24 rows are tiled over CTAs by query position (pos_split)
   return D == 128 && !latent && G <= 8;
 }
 
 namespace {
+
+// Rows per CTA when the query positions are tiled: whole positions of G rows.
+constexpr int kSplitRows = 24;
 
 template <int RB>
 cudaError_t launch_rb(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel<RB>, fast::smem_bytes(RB), smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(a.S * (a.pos_split ? a.T : 1), a.Hkv, a.B);
+  const dim3 grid(a.S * (a.pos_split ? (a.T + a.pos_tile - 1) / a.pos_tile : 1), a.Hkv, a.B);
   fast::decode_fp4_mma_kernel<RB><<<grid, fast::kThreads, fast::smem_bytes(RB), st>>>(a, kmap, vmap);
   return cudaGetLastError();
 }
@@ -655,8 +660,9 @@ cudaError_t launch_rb(const DecodeArgs& a, const CUtensorMap& kmap, const CUtens
 }  // namespace
 
 // Up to 24 query rows per kv head (T * G <= 24, e.g. a T = 3 verify step with
-// G = 8) run in one CTA as 1-3 row blocks; more rows run one CTA per query
-// position (pos_split).
+// G = 8) run in one CTA as 1-3 row blocks; more rows (longer verify blocks,
+// extend steps) are tiled over CTAs of kSplitRows rows' worth of whole
+// positions each (pos_split).
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st) {
   if (D != 128) return cudaErrorNotSupported;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -684,9 +690,14 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   DecodeArgs a = a_in;
-  const int R = a.T * (a.Hq / a.Hkv);
-  a.pos_split = R > 24 ? 1 : 0;
-  if (a.pos_split || R <= 8) return launch_rb<1>(a, kmap, vmap, st);
+  const int G = a.Hq / a.Hkv;
+  int R = a.T * G;
+  a.pos_split = R > kTileRows ? 1 : 0;
+  if (a.pos_split) {
+    a.pos_tile = kSplitRows / G > 0 ? kSplitRows / G : 1;
+    R = a.pos_tile * G;
+  }
+  if (R <= 8) return launch_rb<1>(a, kmap, vmap, st);
   return R <= 16 ? launch_rb<2>(a, kmap, vmap, st) : launch_rb<3>(a, kmap, vmap, st);
 }
 

@@ -61,6 +61,10 @@ CONFIGS = {
     # MTP verify + agentic traffic: ragged 16K..128K contexts, 93 % shared prefix pages, T = 3.
     "verify_agentic": Config("verify_agentic", 32, 3, 64, 8, 128, 16, ("uniform", 16384, 131072),
                              outliers="pct2x16", shared_prefix=0.93, seed=1239),
+    # Extend step: a 512-token chunk of new prompt per sequence over a 32K cached
+    # context (the chunk included), causal among the new tokens.
+    "extend_b4_ctx32k_t512": Config("extend_b4_ctx32k_t512", 4, 512, 64, 8, 128, 16, ("fixed", 32768),
+                                    outliers="pct2x16", seed=1240),
 }
 
 

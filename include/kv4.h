@@ -26,7 +26,12 @@
  *     caller reads it after synchronising.  No kernel traps or waits on
  *     another block.
  *   - Supported: head_dim in {64, 128, 256, 512}; page_size 16; num_q_heads a
- *     multiple of num_kv_heads; q_per_seq (T) in 1..8.
+ *     multiple of num_kv_heads; q_per_seq (T) in 1..KV4_MAX_Q_PER_SEQ.  The
+ *     query rows per kv head, R = T * num_q_heads / num_kv_heads, are
+ *     unlimited for head_dim 128 with at most 8 query heads per kv head
+ *     (4-bit cache without the latent mode, and the FP8 cache); every other
+ *     shape takes R up to 64 (32 at head_dim 256, 16 at 512) and returns
+ *     KV4_ERR_UNSUPPORTED above that.
  *   - Entry points hold no global state and are thread-safe.
  *
  * Cache layout (one block per (page, kv head), blocks page-major:
@@ -69,6 +74,10 @@ typedef enum {
 } kv4_status;
 
 /* Bits written to *dev_error by kernels. */
+/* Largest q_per_seq: decode (1), MTP verify (a few) and extend steps (a
+ * chunk of new tokens over a cached prefix) share one entry point. */
+#define KV4_MAX_Q_PER_SEQ 4096
+
 #define KV4_DEVERR_PAGE 1      /* block_tables entry outside [0, num_pages) */
 #define KV4_DEVERR_CONTEXT 2   /* context_lens[b] outside [q_per_seq, max_pages*page_size] */
 #define KV4_DEVERR_SLOT 4      /* slot_mapping entry outside the cache */
@@ -114,7 +123,10 @@ size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int
 
 /* Paged decode attention over the 4-bit cache ("What is UltraQuant", "Why
  * UltraQuant beats 8-bit KV"; T > 1 is the MTP verify block of
- * "Throughput-latency trade-off").
+ * "Throughput-latency trade-off"; a large T is an extend step, a chunk of
+ * new prompt tokens over a long cached prefix, the prefill side of the
+ * agentic traffic in "Agentic serving" and of the time to first token in
+ * "Key results").
  *   q             device bf16 [batch][q_per_seq][num_q_heads][head_dim], unrotated.
  *                 Query head hq reads kv head hq / (num_q_heads/num_kv_heads).
  *   k_cache       device, layout above.  v_cache: device, or NULL / == k_cache

@@ -74,7 +74,7 @@ def test_host_validation_rejects_before_launch(lib):
                          kw.get("Hq", 8), kw.get("Hkv", 2), kw.get("D", 128), 16, 4, 8, 0.1,
                          kw.get("S", 1), P(4096 * 256), kw.get("ws", 1 << 20), fake, None, None]
     assert dec(*args(Hq=7)) == kv4.KV4_ERR_INVALID_ARG
-    assert dec(*args(T=9)) == kv4.KV4_ERR_UNSUPPORTED
+    assert dec(*args(T=kv4.KV4_MAX_Q_PER_SEQ + 1)) == kv4.KV4_ERR_UNSUPPORTED
     assert dec(*args(D=80)) == kv4.KV4_ERR_UNSUPPORTED
     assert dec(*args(ws=16)) == kv4.KV4_ERR_INVALID_ARG
     assert dec(*args(q=None)) == kv4.KV4_ERR_INVALID_ARG
