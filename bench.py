@@ -42,10 +42,12 @@ sys.path.insert(0, ROOT)
 from bit_kv_cache_rotate_b300 import workloads as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
 DECODE_SOURCES = ("bit_kv_cache_rotate_b300/csrc/kv4_decode_mma.cu",
                   "bit_kv_cache_rotate_b300/csrc/kv4_mma_common.cuh",
                   "bit_kv_cache_rotate_b300/csrc/kv4_decode.h")
 METRIC = "4-bit-KV decode attention: HBM GB/s (% of peak) and ms/step at 32K ctx, batch 32"
+EXTEND_METRIC = "4-bit-KV extend attention: TFLOP/s (% of peak) and ms/step"
 
 
 def kv_bytes_4bit(cfg, lens) -> int:
@@ -53,6 +55,19 @@ def kv_bytes_4bit(cfg, lens) -> int:
     if cfg.latent:
         per_tok //= 2
     return int(np.asarray(lens, dtype=np.int64).sum()) * per_tok
+
+
+def attn_flops(cfg, lens) -> int:
+    """Q.K^T and P.V multiply-adds of one step: position j of a sequence with
+    context L attends to L - T + 1 + j tokens, 4 * D flops per (token, query head)."""
+    T = cfg.q_per_seq
+    lens = np.asarray(lens, dtype=np.int64)
+    visible = T * (lens - T + 1) + T * (T - 1) // 2
+    return int(visible.sum()) * 4 * cfg.head_dim * cfg.num_q_heads
+
+
+def is_extend(cfg) -> bool:
+    return cfg.q_per_seq > 8
 
 
 def kv_bytes_fp8(cfg, lens) -> int:
@@ -83,14 +98,14 @@ def replica_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
     return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
 
 
-def measured_peak():
+def measured_peak(key: str = "hbm_gbs", fallback: float = FALLBACK_HBM_GBS):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
-            return float(json.load(open(p))["hbm_gbs"]), "measured"
+            return float(json.load(open(p))[key]), "measured"
         except Exception:
             pass
-    return FALLBACK_HBM_GBS, "fallback"
+    return fallback, "fallback"
 
 
 def stored_traffic(config_name: str):
@@ -359,12 +374,33 @@ def run_ours(args, rank, world, local_rank):
         fp8_info = {"ms_per_step": round(fms, 5), "GB/s": round(fbytes / (fms * 1e-3) / 1e9, 1),
                     "kv_bytes_per_step": fbytes, "speedup_4bit_vs_fp8": round(fms / ms_per_step, 3)}
 
-    peak, peak_kind = measured_peak()
-    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    flops = attn_flops(cfg, lay.context_lens)
+    extend = is_extend(cfg)
+    if extend:
+        # many positions per sequence: a dense contraction, bound by the tensor pipes
+        peak, peak_kind = measured_peak("bf16_tflops", FALLBACK_BF16_TFLOPS)
+        achieved = flops / (kern_ms * 1e-3) / 1e12
+        metric, unit = EXTEND_METRIC, "TFLOP/s"
+        value = flops * world / (ms_per_step * 1e-3) / 1e12
+        e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "kv4 decode split kernel (query positions tiled over CTAs)",
+                    "achieved": round(achieved, 1), "peak": peak,
+                    "peak_kind": f"{peak_kind} (dense bf16 GEMM, burst; f16 MMAs run at the bf16 rate)",
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": stored_traffic(cfg.name),
+                    "kernel_ms": round(kern_ms, 5)}
+    else:
+        peak, peak_kind = measured_peak()
+        achieved = nbytes / (kern_ms * 1e-3) / 1e9
+        metric, unit = METRIC, "GB/s"
+        e2e_value = replica_gbs(nbytes, world, e2e_ms)
+        roofline = {"bound": "hbm", "kernel": "kv4 decode split kernel", "achieved": round(achieved, 1),
+                    "peak": peak, "peak_kind": f"{peak_kind} (hbm copy)", "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": stored_traffic(cfg.name),
+                    "kernel_ms": round(kern_ms, 5)}
     res = {
-        "metric": METRIC,
+        "metric": metric,
         "value": round(value, 1),
-        "unit": "GB/s",
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -377,15 +413,12 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{cfg.name}: batch {cfg.batch}, ctx {int(lay.context_lens.max())}, "
                                f"{cfg.num_kv_heads} kv heads, {cfg.num_q_heads} q heads, head_dim {cfg.head_dim}, "
                                f"page {cfg.page_size}, T={cfg.q_per_seq}",
-                   "kv_bytes_per_step": nbytes, "num_splits": wl.S,
+                   "kv_bytes_per_step": nbytes, "flops_per_step": flops, "num_splits": wl.S,
                    "l2": "inputs larger than L2 (KV cache per step >> 126 MB)",
                    "launch": "timed steps captured as one CUDA graph (append, decode split, combine per step)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "kv4 decode split kernel", "achieved": round(achieved, 1),
-                     "peak": peak, "peak_kind": f"{peak_kind} (hbm copy)", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": stored_traffic(cfg.name),
-                     "kernel_ms": round(kern_ms, 5)},
-        "e2e": {"value": round(replica_gbs(nbytes, world, e2e_ms), 1), "unit": "GB/s",
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 1), "unit": unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
@@ -506,7 +539,7 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res, wl = run_ours(args, rank, world, local_rank)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not is_extend(wl.cfg):
         res["cpu_baseline"] = cpu_baseline(wl.cfg, wl.lay)
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -43,3 +43,17 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.replica_gbs(2_000_000_000, 1, 1000.0) == pytest.approx(2.0)
+
+
+def test_attention_flop_count_matches_brute_force():
+    """bench.attn_flops: 4 * D flops per (visible token, query head), position j
+    of a sequence with context L seeing L - T + 1 + j tokens."""
+    import dataclasses
+    import bench
+    from bit_kv_cache_rotate_b300 import workloads as W
+    cfg = dataclasses.replace(W.CONFIGS["extend_b4_ctx32k_t512"], q_per_seq=5, num_q_heads=6, head_dim=64)
+    lens = [5, 9, 40]
+    brute = sum(4 * 64 * 6 * (L - 5 + 1 + j) for L in lens for j in range(5))
+    assert bench.attn_flops(cfg, lens) == brute
+    assert bench.is_extend(cfg) is False
+    assert bench.is_extend(W.CONFIGS["extend_b4_ctx32k_t512"]) is True
