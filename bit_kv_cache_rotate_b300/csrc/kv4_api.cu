@@ -198,10 +198,17 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   // measured slower at batch 32, 32K context).
   const char* tc_env = getenv("KV4_DECODE_TCGEN05");
   const bool use_tc = tc_env != nullptr && tc_env[0] == '1';
+  // Extend steps (more query rows than the warp-MMA kernel holds per CTA) run
+  // on the tcgen05 extend kernel; KV4_EXTEND_WARPMMA=1 keeps them on the
+  // warp-MMA kernel's position tiles instead.
+  const char* xw_env = getenv("KV4_EXTEND_WARPMMA");
+  const bool extend_warp = xw_env != nullptr && xw_env[0] == '1';
   a.pos_split = 0;
   a.pos_tile = 1;
   if (!fp8 && use_tc && kv4::tc_path_supported(D, G, T, latent)) {
     e = kv4::launch_decode_tc(a, st);
+  } else if (!fp8 && !extend_warp && kv4::extend_tc_supported(D, G, T, latent)) {
+    e = kv4::launch_extend_tc(a, st);
   } else if (!fp8 && kv4::mla_path_supported(D, G, T, latent)) {
     e = kv4::launch_decode_mla(a, st);
   } else if (!fp8 && kv4::fast_path_supported(D, G, T, latent)) {

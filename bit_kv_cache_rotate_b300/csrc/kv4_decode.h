@@ -53,5 +53,7 @@ bool tc_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 bool fp8_fast_path_supported(int D, int G, int T);
 cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st);
+bool extend_tc_supported(int D, int G, int T, bool latent);
+cudaError_t launch_extend_tc(const DecodeArgs& a, cudaStream_t st);
 
 }  // namespace kv4

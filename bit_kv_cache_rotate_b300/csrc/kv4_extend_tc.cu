@@ -1,0 +1,689 @@
+// kv4_extend_tc.cu -- extend attention over the 4-bit cache on the tcgen05
+// tensor cores (sm_103a), head_dim 128, 1, 2, 4 or 8 query heads per kv head.
+//
+// An extend step is a chunk of new prompt tokens per sequence: T query
+// positions attend to the cached prefix and causally to each other ("Agentic
+// serving": long shared prefixes, short new turns; the time to first token of
+// "Key results").  With 128 query rows per CTA (128 / G positions of G query
+// heads each) both products are real tiles, so they go to tcgen05.mma with the
+// accumulators in tensor memory:
+//
+//   Q.K^T  S[row][token] (M = 128 rows, N = 128 tokens = 8 pages, K = 128
+//          channels), kind::mxf4 block-scaled ("What is UltraQuant": FP4 codes
+//          and power-of-two scales straight into the matrix units).  B = the
+//          cache's K codes as stored (its 8-token x 32-channel tiles are the
+//          MMA's core matrices, brought in by tensor gathers), scale B = the
+//          cache's UE8M0 bytes.  A = q, rotated and times softmax scale and
+//          log2 e, as 11 E2M1 terms with one UE8M0 scale per 32 channels each
+//          (each term codes the remainder of the ones before it, a factor of
+//          at least 4 smaller); the terms accumulate into the same S, 22 MMAs
+//          per chunk, and carry q to about 2^-22 of each 32-channel block's
+//          largest element (8 terms, 2^-16, left errors near 2e-3 at 32K).
+//   softmax one thread per row: S comes out of tensor memory row by row; online
+//          softmax with a lazy maximum (the reference moves only when a logit
+//          exceeds it by more than 8, log2 units).
+//   P.V    O[row][dim] (M = 128, N = 128 dims, K = 16 tokens per MMA),
+//          kind::f16.  B = V widened to f16 once per chunk by the CUDA cores
+//          (hardware E2M1->f16 conversion times 2^(e - E_c), E_c the chunk's
+//          largest V scale exponent, so the f16 values are exact from 2^-22 of
+//          the chunk maximum up); A = P' = p * 2^(E_c - E_ref) as f16 hi +
+//          f16 remainder (lo), two MMAs per k-step, so P carries about 22 bits.
+//          E_ref moves (and O is rescaled in tensor memory) only when a chunk's
+//          E_c exceeds it by more than 4, or with the softmax reference.
+//
+// One CTA per (split, position tile, kv head, sequence), 4 warps; 199 KB of
+// shared memory and 512 tensor-memory columns, so one CTA per SM.  The K and V
+// pages of chunk c + 2 stream in by tensor gathers while chunk c is processed.
+// Every wait is bounded; a timeout is agreed at a CTA barrier, flagged as
+// KV4_DEVERR_TIMEOUT, and the kernel drains its copies and MMAs, frees its
+// tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+#include <mutex>
+#include <type_traits>
+
+#include "kv4_common.cuh"
+#include "kv4_decode.h"
+#include "kv4_mma_common.cuh"
+
+namespace kv4 {
+namespace ext {
+
+using namespace kv4::mma;
+
+constexpr int D = 128;
+constexpr int kThreads = 128;
+constexpr int kRows = 128;                            // query rows per CTA (MMA M)
+constexpr int kChunkPages = 8;
+constexpr int kChunk = kChunkPages * kPage;           // 128 tokens (Q.K^T N, P.V K)
+constexpr int kTerms = 11;                            // q terms: about 2^-22 of each block's largest element
+constexpr int kCodeBytes = kPage * D / 2;             // 1024
+constexpr int kBlk = kCodeBytes + kPage * D / 32;     // 1088
+
+// shared memory map (bytes; operand tiles 128-byte aligned)
+constexpr int kQTerm = kRows * D / 2;                 // one q term: 128 rows x 64 B
+constexpr int kOffQ = 0;                              // [kTerms]
+constexpr int kKC = kChunkPages * kCodeBytes;         // K codes of a chunk
+constexpr int kOffKC = kOffQ + kTerms * kQTerm;       // [2 buffers]
+constexpr int kKS = kChunkPages * 64;                 // K scales of a chunk [8 pages][16 tokens][4]
+constexpr int kOffKS = kOffKC + 2 * kKC;              // [2 buffers]
+constexpr int kVR = kChunkPages * kBlk;               // V blocks of a chunk, as cached
+constexpr int kOffVR = kOffKS + 2 * kKS;              // [2 buffers]
+constexpr int kVF = D * kChunk * 2;                   // V' f16, 128 dims x 128 tokens
+constexpr int kOffVF = kOffVR + 2 * kVR;
+constexpr int kPF = kRows * kChunk * 2;               // P' f16, 128 rows x 128 tokens
+constexpr int kOffP = kOffVF + kVF;                   // [hi, lo]
+constexpr int kOffFac = kOffP + 2 * kPF;              // f16 [4 groups][128 tokens] V factors
+constexpr int kOffSfa = kOffFac + 4 * kChunk * 2;     // [kTerms][128 rows][4 groups] q scale bytes
+constexpr int kOffMisc = kOffSfa + kTerms * kRows * 4;  // [4] per-warp maxima
+constexpr int kOffBar = kOffMisc + 64;                // full[2], sdone, pvdone
+constexpr int kSmem = kOffBar + 8 * 4;
+static_assert(kOffKC % 1024 == 0 && kOffKS % 128 == 0 && kOffVR % 128 == 0 && (kOffVR + kVR) % 128 == 0 &&
+                  kOffVF % 128 == 0 && kOffP % 128 == 0 && kOffFac % 16 == 0 && kOffBar % 8 == 0,
+              "operand and copy alignment");
+static_assert(kSmem <= 227 * 1024 && kSmem > 227 * 1024 / 2, "one CTA per SM (all 512 tensor-memory columns)");
+
+// tensor memory columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;      // S: 128 columns (tokens)
+constexpr uint32_t kColO = 128;    // O of the current segment of chunks: 128 columns (dims)
+constexpr uint32_t kColOm = 256;   // O of the segments before, summed by the CUDA cores
+constexpr uint32_t kColSfa = 384;  // [11 terms][2 k-steps][4]
+constexpr uint32_t kColSfb = 472;  // [2 buffers][2 k-steps][4]
+// The tensor core's own accumulation of O is kept to kFold chunks (kFold * 16
+// MMAs): a segment is then added into the running O by the CUDA cores (fp32,
+// round to nearest).  One accumulator over a 32K context (4096 MMAs) measured
+// about four times the output error.
+constexpr int kFold = 8;
+
+// kind::mxf4 (A = B = E2M1, UE8M0 scales), M = 128, N = 128; kind::f16 (f16
+// operands, fp32 accumulate), M = 128, N = 128.  Both K-major.
+constexpr uint32_t kIdescQK =
+    (1u << 7) | (1u << 10) | ((uint32_t)(kChunk >> 3) << 17) | (1u << 23) | ((uint32_t)(kRows >> 4) << 24);
+constexpr uint32_t kIdescPV = (1u << 4) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+
+// K-major, no swizzle: core matrices of 8 rows x 16 B; LBO (next core matrix
+// along K) 128 B, SBO (next 8 rows) sbo; descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         (1ull << 46);
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(kIdescQK), "r"(sfa), "r"(sfb), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(kIdescPV), "r"(accumulate));
+}
+
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st4(uint32_t addr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v0), "r"(v1),
+               "r"(v2), "r"(v3));
+}
+
+// 32 consecutive columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(addr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(addr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2,
+                                            int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+struct Maps {
+  CUtensorMap kcodes;  // K blocks, first 1024 bytes of each (128 eight-byte elements)
+  CUtensorMap kscale;  // K blocks, the 64 scale bytes (elements 128..135)
+  CUtensorMap vblock;  // V blocks, whole (136 elements)
+};
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    extend_fp4_tc_kernel(DecodeArgs a, const __grid_constant__ Maps maps) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint32_t tmem_base_s;
+  const int G = a.Hq / a.Hkv;
+  const int PT = kRows / G;  // positions per tile
+  const int n_tiles = (a.T + PT - 1) / PT;
+  const int s = (int)blockIdx.x / n_tiles;
+  const int j0 = ((int)blockIdx.x % n_tiles) * PT;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int Tc = min(PT, a.T - j0);
+  const int R = Tc * G;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int L_seq = a.context_lens[b];
+  // tokens visible to the tile's last position; row r (position j0 + r / G)
+  // sees the first L - Tc + 1 + r / G of them
+  const int L = L_seq - (a.T - Tc) + j0;
+  const size_t row0 = ((size_t)b * a.T + j0) * a.Hq;
+  auto row_index = [&](int r) -> size_t { return row0 + (size_t)(r / G) * a.Hq + h * G + (r % G); };
+  auto write_empty = [&]() {
+    for (int r = w; r < R; r += 4) {
+      const size_t rr = row_index(r) * a.S + s;
+      for (int d = lane; d < D; d += 32) a.part_o[rr * D + d] = 0.0f;
+      if (lane == 0) a.part_lse[rr] = -INFINITY;
+    }
+  };
+  if (L_seq < a.T || L_seq > a.max_pages * kPage) {
+    if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
+    write_empty();
+    return;
+  }
+  const int n_pages = (L + kPage - 1) / kPage;
+  const int per = (n_pages + a.S - 1) / a.S;
+  const int p0 = s * per;
+  const int p1 = min(n_pages, p0 + per);
+  if (p0 >= p1) {
+    write_empty();
+    return;
+  }
+  const int n_chunks = (p1 - p0 + kChunkPages - 1) / kChunkPages;
+  const int32_t* table = a.block_tables + (size_t)b * a.max_pages;
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* full = bars;        // [2]: one chunk's K codes, K scales and V blocks
+  uint64_t* sdone = bars + 2;   // Q.K^T of a chunk complete
+  uint64_t* pvdone = bars + 3;  // P.V of a chunk complete
+  int* wmax = reinterpret_cast<int*>(smem + kOffMisc);
+
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (w == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_s)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t tmem_lane = tmem + ((uint32_t)(32 * w) << 16);
+
+  // chunk c -> buffer c & 1: four tensor gathers for K (codes, scales of 8
+  // pages), two for V; pages past the split re-read the chunk's first page
+  // (masked like tokens past the context).  Issued by thread 0.
+  auto issue = [&](int c) {
+    const int buf = c & 1;
+    const int pg = p0 + c * kChunkPages;
+    const int nv = min(kChunkPages, p1 - pg);
+    int rows[kChunkPages];
+#pragma unroll
+    for (int i = 0; i < kChunkPages; ++i) {
+      int page = 0;
+      if (i < nv) {
+        page = table[pg + i];
+        if (page < 0 || page >= a.num_pages) {
+          flag_error(a.dev_error, KV4_DEVERR_PAGE);
+          page = 0;
+        }
+      }
+      rows[i] = i < nv ? page * a.Hkv + h : rows[0];
+    }
+    uint64_t* bar = &full[buf];
+    mbar_expect_tx(bar, (uint32_t)(kChunkPages * (kCodeBytes + 64 + kBlk)));
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int* r4 = rows + 4 * q;
+      tma_gather4(sbase + kOffKC + buf * kKC + q * 4 * kCodeBytes, &maps.kcodes, 0, r4[0], r4[1], r4[2], r4[3], bar);
+      tma_gather4(sbase + kOffKS + buf * kKS + q * 4 * 64, &maps.kscale, kCodeBytes / 8, r4[0], r4[1], r4[2], r4[3],
+                  bar);
+      tma_gather4(sbase + kOffVR + buf * kVR + q * 4 * kBlk, &maps.vblock, 0, r4[0], r4[1], r4[2], r4[3], bar);
+    }
+  };
+  // copies and MMAs issued (thread 0's counts) for the drain after a timeout
+  int issued = 0, qk_issued = 0, pv_issued = 0;
+  if (tid == 0) {
+    fence_proxy_async();
+    issue(0);
+    if (n_chunks > 1) issue(1);
+    issued = min(n_chunks, 2);
+  }
+
+  // ---- q prologue: rotate (fp32 butterfly), times softmax_scale*log2e/sqrt(D),
+  // then 11 E2M1 terms with one UE8M0 scale per 32 channels each.  Row r of
+  // term j: core-matrix row group r/8, channel block lane/8, bytes 2*(lane%8).
+  uint8_t* sfa_s = smem + kOffSfa;  // [term][row][block]
+  for (int r = w; r < kRows; r += 4) {
+    float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (r < R) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(a.q + row_index(r) * D + lane * 4);
+      x[0] = bf16_bits_to_float(raw.x & 0xFFFFu);
+      x[1] = bf16_bits_to_float(raw.x >> 16);
+      x[2] = bf16_bits_to_float(raw.y & 0xFFFFu);
+      x[3] = bf16_bits_to_float(raw.y >> 16);
+      fwht_warp<4, float>(x);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] *= a.qscale;
+    }
+#pragma unroll 1
+    for (int term = 0; term < kTerms; ++term) {
+      float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+      // block exponent: the smallest e with am <= 6 * 2^e (no saturation)
+      int e = -125;
+      const uint32_t ab = __float_as_uint(am);
+      if (am >= 1.0e-30f) {
+        const int e0 = (int)(ab >> 23) - 127;
+        e = (ab & 0x7FFFFFu) <= 0x400000u ? e0 - 2 : e0 - 1;
+        e = max(-125, min(125, e));
+      }
+      const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+      const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+      const uint32_t c01 = f32x2_to_e2m1x2(x[0] * down, x[1] * down);
+      const uint32_t c23 = f32x2_to_e2m1x2(x[2] * down, x[3] * down);
+      const uint32_t h01 = e2m1x2_to_f16x2(c01, 0), h23 = e2m1x2_to_f16x2(c23, 0);
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+      x[0] -= f01.x * up;
+      x[1] -= f01.y * up;
+      x[2] -= f23.x * up;
+      x[3] -= f23.y * up;
+      uint8_t* dst = smem + kOffQ + term * kQTerm + ((r >> 3) * 4 + (lane >> 3)) * 128 + (r & 7) * 16 + 2 * (lane & 7);
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(c01 | (c23 << 8));
+      if ((lane & 7) == 0) sfa_s[(term * kRows + r) * 4 + (lane >> 3)] = (uint8_t)(e + 127);
+    }
+  }
+  __syncthreads();
+  // q scale factors into tensor memory, replicated in every lane quadrant:
+  // column c0 + i of lane l holds row 32i + l (the MMA reads row m at lane m,
+  // column c0 + m/32).
+#pragma unroll 1
+  for (int term = 0; term < kTerms; ++term)
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint8_t* sb = sfa_s + (term * kRows + 32 * i + lane) * 4 + 2 * ks;
+        v[i] = (uint32_t)sb[0] | ((uint32_t)sb[1] << 8) | 0x7F7F0000u;
+      }
+      tmem_st4(tmem_lane + kColSfa + (term * 2 + ks) * 4, v[0], v[1], v[2], v[3]);
+    }
+  {
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tmem_st32(tmem_lane + kColOm + 32 * q, z);
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  fence_proxy_async();  // q terms written by ordinary stores, read by the MMA
+
+  // this thread's row
+  const int my_r = tid;
+  const int my_limit = my_r < R ? L - Tc + 1 + my_r / G : 0;
+  float m_run = -INFINITY, l_run = 0.0f;
+  int e_ref = 0;  // V scale reference (UE8M0 byte value)
+  bool timed_out = false;
+  int waited_full = 0;
+
+  __half* fac = reinterpret_cast<__half*>(smem + kOffFac);  // [4][128]
+
+#pragma unroll 1
+  for (int c = 0; c < n_chunks; ++c) {
+    const int buf = c & 1;
+    const int pg = p0 + c * kChunkPages;
+    const int nv = min(kChunkPages, p1 - pg);
+    // ---- wait for the chunk's pages
+    if (!mbar_wait(&full[buf], (uint32_t)((c >> 1) & 1))) timed_out = true;
+    if (__syncthreads_or(timed_out)) {
+      timed_out = true;
+      break;
+    }
+    waited_full = c + 1;
+    // ---- K scales into tensor memory (token 32i + lane at column c0 + i of
+    // every quadrant), and the V scale factors of the chunk
+    {
+      uint32_t v0[4], v1[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = 32 * i + lane, pi = n >> 4, tk = n & 15;
+        const bool ok = pi < nv && (pg + pi) * kPage + tk < L;
+        const uint32_t sw = ok ? *reinterpret_cast<const uint32_t*>(smem + kOffKS + buf * kKS + pi * 64 + tk * 4)
+                               : 0x7F7F7F7Fu;
+        v0[i] = (sw & 0xFFFFu) | 0x7F7F0000u;
+        v1[i] = (sw >> 16) | 0x7F7F0000u;
+      }
+      tmem_st4(tmem_lane + kColSfb + buf * 8 + 0, v0[0], v0[1], v0[2], v0[3]);
+      tmem_st4(tmem_lane + kColSfb + buf * 8 + 4, v1[0], v1[1], v1[2], v1[3]);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    // token tid of the chunk: its 4 V scale bytes
+    const int vpi = tid >> 4, vtk = tid & 15;
+    const bool vok = vpi < nv && (pg + vpi) * kPage + vtk < L;
+    const uint32_t vsw = vok ? *reinterpret_cast<const uint32_t*>(smem + kOffVR + buf * kVR + vpi * kBlk +
+                                                                  kCodeBytes + vtk * 4)
+                             : 0u;
+    {
+      uint32_t m4 = __vmaxu4(vsw, vsw >> 16);
+      m4 = max(m4 & 0xFFu, (m4 >> 8) & 0xFFu);
+      m4 = __reduce_max_sync(0xffffffffu, m4);
+      if (lane == 0) wmax[w] = (int)m4;
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    // ---- Q.K^T of the chunk (one thread issues; the others go on to V)
+    if (tid == 0) {
+      const uint32_t kb = sbase + kOffKC + buf * kKC;
+#pragma unroll
+      for (int term = 0; term < kTerms; ++term)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma_mxf4(tmem + kColS, smem_desc(sbase + kOffQ + term * kQTerm + ks * 256, 512),
+                   smem_desc(kb + ks * 256, 512), tmem + kColSfa + (term * 2 + ks) * 4,
+                   tmem + kColSfb + buf * 8 + ks * 4, (term | ks) != 0);
+      commit(sdone);
+      ++qk_issued;
+    }
+    const int e_c = max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3]));
+    // V reference: set by the first chunk, raised when a chunk exceeds it by > 4
+    float o_fac = 1.0f;
+    if (c == 0) {
+      e_ref = e_c;
+    } else if (e_c > e_ref + 4) {
+      const int dd = e_ref - e_c;
+      o_fac = dd > -127 ? __uint_as_float((uint32_t)(127 + dd) << 23) : 0.0f;
+      e_ref = e_c;
+    }
+    // exponent of the chunk's V': at most 30 below the reference, so that
+    // p' = p * 2^(E_x - E_ref) cannot underflow while p still counts in l
+    // (groups more than 22 binades below E_x widen to zero: negligible values)
+    const int e_x = max(e_c, e_ref - 30);
+    // V factors 2^(e - E_x) as f16 (0 for tokens past the split or context)
+#pragma unroll
+    for (int g4 = 0; g4 < 4; ++g4) {
+      const int e = (int)((vsw >> (8 * g4)) & 0xFFu) - e_x;  // <= 0
+      const float f = (vok && e >= -126) ? __uint_as_float((uint32_t)(127 + e) << 23) : 0.0f;
+      fac[g4 * kChunk + tid] = __float2half_rn(f);
+    }
+    __syncthreads();  // factors visible; P.V of the previous chunk was waited on
+    // ---- V' (dim tid, all 128 tokens of the chunk) -> canonical K-major tile
+    {
+      const int d = tid, g4 = d >> 5;
+      const uint8_t* vr = smem + kOffVR + buf * kVR + d * 8;
+      const uint4* fr = reinterpret_cast<const uint4*>(fac + g4 * kChunk);
+#pragma unroll 2
+      for (int pi = 0; pi < kChunkPages; ++pi) {
+        const uint2 wv = *reinterpret_cast<const uint2*>(vr + pi * kBlk);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t word = hh ? wv.y : wv.x;
+          const uint4 f = fr[pi * 2 + hh];
+          uint4 o;
+          o.x = hmul2(e2m1x2_to_f16x2(word, 0), f.x);
+          o.y = hmul2(e2m1x2_to_f16x2(word, 1), f.y);
+          o.z = hmul2(e2m1x2_to_f16x2(word, 2), f.z);
+          o.w = hmul2(e2m1x2_to_f16x2(word, 3), f.w);
+          *reinterpret_cast<uint4*>(smem + kOffVF + ((d >> 3) * 16 + pi * 2 + hh) * 128 + (d & 7) * 16) = o;
+        }
+      }
+    }
+    // ---- S of the chunk
+    if (!mbar_wait(sdone, (uint32_t)(c & 1))) timed_out = true;
+    if (__any_sync(0xffffffffu, timed_out)) timed_out = true;
+    fence_after_sync();
+    // the chunk's buffers are free once Q.K^T is done and V' is built: refill
+    // after the barrier below
+    // tokens 0 .. nvr-1 of the chunk are visible to this row (the chunk's
+    // positions are consecutive); whole warps with every token visible skip the
+    // per-token test
+    const int nvr = max(0, min(nv * kPage, my_limit - pg * kPage));
+    const bool all_full = __all_sync(0xffffffffu, nvr == kChunk);
+    const uint32_t s_addr = tmem_lane + kColS;
+    float cmx = -INFINITY;
+    auto row_max = [&](auto masked) {
+      constexpr bool M = decltype(masked)::value;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t sv[32];
+        tmem_ld32(s_addr + 32 * q, sv);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int lim = nvr - 32 * q;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = __uint_as_float(sv[i]);
+          m4[i & 3] = fmaxf(m4[i & 3], (!M || i < lim) ? x : -INFINITY);
+        }
+        cmx = fmaxf(cmx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+      }
+    };
+    if (!timed_out) {
+      if (all_full) row_max(std::false_type{});
+      else row_max(std::true_type{});
+    }
+    const float m_new = cmx > m_run + 8.0f ? cmx : m_run;
+    const float alpha = m_new == m_run ? 1.0f : ex2(m_run - m_new);
+    m_run = m_new;
+    // p' = 2^(s - m + E_x - E_ref): the V factor folded into the exponent (a
+    // row with nothing visible yet gets p' = 0)
+    const float shift = m_new == -INFINITY ? -INFINITY : (float)(e_x - e_ref) - m_new;
+    float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    auto write_p = [&](auto masked) {
+      constexpr bool M = decltype(masked)::value;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t sv[32];
+        tmem_ld32(s_addr + 32 * q, sv);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int lim = nvr - 32 * q;
+#pragma unroll
+        for (int o8 = 0; o8 < 4; ++o8) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2) {
+            const int i = o8 * 8 + i2 * 2;
+            float x0 = __uint_as_float(sv[i]), x1 = __uint_as_float(sv[i + 1]);
+            if (M) {
+              x0 = i < lim ? x0 : -INFINITY;
+              x1 = i + 1 < lim ? x1 : -INFINITY;
+            }
+            const float p0 = ex2(x0 + shift), p1 = ex2(x1 + shift);
+            ls4[i2] += p0 + p1;
+            hw[i2] = pack_f16x2(p0, p1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[i2]));
+            lw[i2] = pack_f16x2(p0 - hf.x, p1 - hf.y);
+          }
+          const int k8 = q * 4 + o8;  // token octet
+          const int off = ((my_r >> 3) * 16 + k8) * 128 + (my_r & 7) * 16;
+          *reinterpret_cast<uint4*>(smem + kOffP + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(smem + kOffP + kPF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+    };
+    if (!timed_out) {
+      if (all_full) write_p(std::false_type{});
+      else write_p(std::true_type{});
+    }
+    const float lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+    // l in the units of p (not p'): p = p' * 2^(E_ref - E_x), E_ref - E_x in [-4, 30]
+    l_run = l_run * alpha + lsum * __uint_as_float((uint32_t)(127 + e_ref - e_x) << 23);
+    // ---- fold the segment into the running O: at the end of a segment, and
+    // whenever the softmax or V reference moved (the fold applies the factor)
+    const float f_row = alpha * o_fac;
+    if (c > 0 && !timed_out && __any_sync(0xffffffffu, f_row != 1.0f || c % kFold == 0)) {
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t ov[32], om[32];
+        tmem_ld32(tmem_lane + kColO + 32 * q, ov);
+        tmem_ld32(tmem_lane + kColOm + 32 * q, om);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          om[i] = __float_as_uint((__uint_as_float(om[i]) + __uint_as_float(ov[i])) * f_row);
+          ov[i] = 0u;
+        }
+        tmem_st32(tmem_lane + kColOm + 32 * q, om);
+        tmem_st32(tmem_lane + kColO + 32 * q, ov);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    fence_proxy_async();  // P' and V' written by ordinary stores, read by the MMA
+    fence_before_sync();
+    if (__syncthreads_or(timed_out)) {
+      timed_out = true;
+      break;
+    }
+    fence_after_sync();
+    // ---- P.V of the chunk; then refill the chunk's buffers with chunk c + 2
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < kChunk / 16; ++ks) {
+        const uint64_t vd = smem_desc(sbase + kOffVF + ks * 256, 2048);
+        mma_f16(tmem + kColO, smem_desc(sbase + kOffP + ks * 256, 2048), vd, (c | ks) != 0);
+        mma_f16(tmem + kColO, smem_desc(sbase + kOffP + kPF + ks * 256, 2048), vd, 1);
+      }
+      commit(pvdone);
+      ++pv_issued;
+      if (c + 2 < n_chunks) {
+        fence_proxy_async();
+        issue(c + 2);
+        issued = c + 3;
+      }
+    }
+    // V' and P' are rewritten by the next chunk: wait for this P.V
+    if (!mbar_wait(pvdone, (uint32_t)(c & 1))) timed_out = true;
+    fence_after_sync();
+    if (__syncthreads_or(timed_out)) {
+      timed_out = true;
+      break;
+    }
+  }
+
+  if (timed_out) {
+    // Stop, but let every copy and MMA this CTA issued finish before the
+    // shared and tensor memory are released (each wait again bounded).
+    if (tid == 0) {
+      flag_error(a.dev_error, KV4_DEVERR_TIMEOUT);
+      for (int c = waited_full; c < issued; ++c) (void)mbar_wait(&full[c & 1], (uint32_t)((c >> 1) & 1));
+      if (qk_issued > 0) (void)mbar_wait(sdone, (uint32_t)((qk_issued - 1) & 1));
+      if (pv_issued > 0) (void)mbar_wait(pvdone, (uint32_t)((pv_issued - 1) & 1));
+    }
+    fence_before_sync();
+    __syncthreads();
+  } else {
+    // ---- this split's output of row tid: O * 2^(E_ref - 127) / l (rotated
+    // space); the loads are warp-collective, rows past R only skip the stores
+    const bool valid_row = my_r < R;
+    const size_t rr = valid_row ? row_index(my_r) * a.S + s : 0;
+    float* dst = a.part_o + rr * D;
+    const bool any = l_run > 0.0f;
+    const float sc = any ? __uint_as_float((uint32_t)e_ref << 23) / l_run : 0.0f;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t ov[32], om[32];
+      tmem_ld32(tmem_lane + kColO + 32 * q, ov);
+      tmem_ld32(tmem_lane + kColOm + 32 * q, om);
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      if (valid_row) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float4 o4;
+          o4.x = (__uint_as_float(om[i]) + __uint_as_float(ov[i])) * sc;
+          o4.y = (__uint_as_float(om[i + 1]) + __uint_as_float(ov[i + 1])) * sc;
+          o4.z = (__uint_as_float(om[i + 2]) + __uint_as_float(ov[i + 2])) * sc;
+          o4.w = (__uint_as_float(om[i + 3]) + __uint_as_float(ov[i + 3])) * sc;
+          *reinterpret_cast<float4*>(dst + 32 * q + i) = o4;
+        }
+      }
+    }
+    if (valid_row) a.part_lse[rr] = any ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    fence_before_sync();
+    __syncthreads();
+  }
+  if (w == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+}  // namespace ext
+
+bool extend_tc_supported(int D, int G, int T, bool latent) {
+  return D == 128 && !latent && (G == 1 || G == 2 || G == 4 || G == 8) && T * G > kTileRows;
+}
+
+cudaError_t launch_extend_tc(const DecodeArgs& a, cudaStream_t st) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) return cudaErrorNotSupported;
+  // Each cache as a 2-D tensor of (page, head) blocks: 136 eight-byte elements
+  // per row, row stride 1088 bytes.  Boxes of one row (gather4).
+  ext::Maps maps;
+  const cuuint64_t dims[2] = {(cuuint64_t)ext::kBlk / 8, (cuuint64_t)a.num_pages * a.Hkv};
+  const cuuint64_t strides[1] = {(cuuint64_t)ext::kBlk};
+  const cuuint32_t estr[2] = {1, 1};
+  struct {
+    CUtensorMap* map;
+    const uint8_t* base;
+    cuuint32_t box0;
+  } spec[3] = {{&maps.kcodes, a.k_cache, ext::kCodeBytes / 8},
+               {&maps.kscale, a.k_cache, 8},
+               {&maps.vblock, a.v_cache, ext::kBlk / 8}};
+  for (auto& sp : spec) {
+    const cuuint32_t box[2] = {sp.box0, 1};
+    if (encode(sp.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(sp.base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static std::atomic<unsigned long long> smem_set{0};
+  const cudaError_t e = set_smem_limit_once(ext::extend_fp4_tc_kernel, ext::kSmem, smem_set);
+  if (e != cudaSuccess) return e;
+  const int G = a.Hq / a.Hkv;
+  const int PT = ext::kRows / G;
+  const dim3 grid(a.S * ((a.T + PT - 1) / PT), a.Hkv, a.B);
+  ext::extend_fp4_tc_kernel<<<grid, ext::kThreads, ext::kSmem, st>>>(a, maps);
+  return cudaGetLastError();
+}
+
+}  // namespace kv4

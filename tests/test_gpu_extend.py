@@ -5,6 +5,7 @@ CTAs; each CTA is checked through the whole output against the oracle's fp64
 attention (max abs error 2e-3), across tile boundaries, ragged contexts,
 split counts, GQA groups and the pure-prefill case (context == chunk)."""
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -93,3 +94,14 @@ def test_extend_split_counts(S):
 def test_extend_fp8_comparator():
     err = _run(_cfg(30, ("uniform", 300, 800)), fp8=True)
     assert err <= TOL, f"max abs error {err:.3e}"
+
+
+@pytest.mark.parametrize("warp", [False, True])
+def test_extend_both_kernels(warp, monkeypatch):
+    """G = 8 and 4 on the tcgen05 extend kernel (default) and on the warp-MMA
+    kernel's position tiles (KV4_EXTEND_WARPMMA=1)."""
+    if warp:
+        monkeypatch.setenv("KV4_EXTEND_WARPMMA", "1")
+    for Hq, Hkv, T, ctx in [(64, 8, 48, ("uniform", 300, 1100)), (16, 4, 130, ("uniform", 200, 700))]:
+        err = _run(_cfg(T, ctx, Hq=Hq, Hkv=Hkv))
+        assert err <= TOL, (warp, Hq, Hkv, T, err)
