@@ -55,7 +55,8 @@ namespace ext {
 using namespace kv4::mma;
 
 constexpr int D = 128;
-constexpr int kThreads = 128;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
 constexpr int kRows = 128;                            // query rows per CTA (MMA M)
 constexpr int kChunkPages = 8;
 constexpr int kChunk = kChunkPages * kPage;           // 128 tokens (Q.K^T N, P.V K)
@@ -178,10 +179,15 @@ struct Maps {
 };
 
 // ---------------------------------------------------------------- kernel
+// Warp w serves the 32 rows of lane quadrant w % 4 (the tensor-memory lanes it
+// may access) and half w / 4 of the columns: tokens 64h .. 64h + 63 of S and
+// dims 64h .. 64h + 63 of O.  The two warps of a quadrant exchange their row
+// maxima and sums through shared memory.
 __global__ void __launch_bounds__(kThreads, 1)
     extend_fp4_tc_kernel(DecodeArgs a, const __grid_constant__ Maps maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint32_t tmem_base_s;
+  __shared__ float xch_s[2][kRows];
   const int G = a.Hq / a.Hkv;
   const int PT = kRows / G;  // positions per tile
   const int n_tiles = (a.T + PT - 1) / PT;
@@ -191,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Tc = min(PT, a.T - j0);
   const int R = Tc * G;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int qd = w & 3, hf = w >> 2;
   const int L_seq = a.context_lens[b];
   // tokens visible to the tile's last position; row r (position j0 + r / G)
   // sees the first L - Tc + 1 + r / G of them
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t row0 = ((size_t)b * a.T + j0) * a.Hq;
   auto row_index = [&](int r) -> size_t { return row0 + (size_t)(r / G) * a.Hq + h * G + (r % G); };
   auto write_empty = [&]() {
-    for (int r = w; r < R; r += 4) {
+    for (int r = w; r < R; r += kWarps) {
       const size_t rr = row_index(r) * a.S + s;
       for (int d = lane; d < D; d += 32) a.part_o[rr * D + d] = 0.0f;
       if (lane == 0) a.part_lse[rr] = -INFINITY;
@@ -239,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t tmem_lane = tmem + ((uint32_t)(32 * w) << 16);
+  const uint32_t tmem_lane = tmem + ((uint32_t)(32 * qd) << 16);
 
   // chunk c -> buffer c & 1: four tensor gathers for K (codes, scales of 8
   // pages), two for V; pages past the split re-read the chunk's first page
@@ -282,10 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- q prologue: rotate (fp32 butterfly), times softmax_scale*log2e/sqrt(D),
-  // then 11 E2M1 terms with one UE8M0 scale per 32 channels each.  Row r of
-  // term j: core-matrix row group r/8, channel block lane/8, bytes 2*(lane%8).
+  // then kTerms E2M1 terms with one UE8M0 scale per 32 channels each.  Row r
+  // of term j: core-matrix row group r/8, channel block lane/8, bytes 2*(lane%8).
   uint8_t* sfa_s = smem + kOffSfa;  // [term][row][block]
-  for (int r = w; r < kRows; r += 4) {
+  for (int r = w; r < kRows; r += kWarps) {
     float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     if (r < R) {
       const uint2 raw = *reinterpret_cast<const uint2*>(a.q + row_index(r) * D + lane * 4);
@@ -330,38 +337,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // q scale factors into tensor memory, replicated in every lane quadrant:
   // column c0 + i of lane l holds row 32i + l (the MMA reads row m at lane m,
-  // column c0 + m/32).
+  // column c0 + m/32).  The running O starts at zero.
+  if (hf == 0) {
 #pragma unroll 1
-  for (int term = 0; term < kTerms; ++term)
+    for (int term = 0; term < kTerms; ++term)
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      uint32_t v[4];
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t v[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint8_t* sb = sfa_s + (term * kRows + 32 * i + lane) * 4 + 2 * ks;
-        v[i] = (uint32_t)sb[0] | ((uint32_t)sb[1] << 8) | 0x7F7F0000u;
+        for (int i = 0; i < 4; ++i) {
+          const uint8_t* sb = sfa_s + (term * kRows + 32 * i + lane) * 4 + 2 * ks;
+          v[i] = (uint32_t)sb[0] | ((uint32_t)sb[1] << 8) | 0x7F7F0000u;
+        }
+        tmem_st4(tmem_lane + kColSfa + (term * 2 + ks) * 4, v[0], v[1], v[2], v[3]);
       }
-      tmem_st4(tmem_lane + kColSfa + (term * 2 + ks) * 4, v[0], v[1], v[2], v[3]);
-    }
+  }
   {
     uint32_t z[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) z[i] = 0u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tmem_st32(tmem_lane + kColOm + 32 * q, z);
+    for (int q = 0; q < 2; ++q) tmem_st32(tmem_lane + kColOm + 64 * hf + 32 * q, z);
   }
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   fence_proxy_async();  // q terms written by ordinary stores, read by the MMA
 
-  // this thread's row
-  const int my_r = tid;
+  // this thread's row and column half
+  const int my_r = 32 * qd + lane;
   const int my_limit = my_r < R ? L - Tc + 1 + my_r / G : 0;
-  float m_run = -INFINITY, l_run = 0.0f;
-  int e_ref = 0;  // V scale reference (UE8M0 byte value)
+  float m_run = -INFINITY;
+  float l_half = 0.0f;  // this half's share of the row sum
+  int e_ref = 0;        // V scale reference (UE8M0 byte value)
   bool timed_out = false;
   int waited_full = 0;
-
   __half* fac = reinterpret_cast<__half*>(smem + kOffFac);  // [4][128]
+  const uint32_t s_addr = tmem_lane + kColS + 64 * hf;
 
 #pragma unroll 1
   for (int c = 0; c < n_chunks; ++c) {
@@ -376,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     waited_full = c + 1;
     // ---- K scales into tensor memory (token 32i + lane at column c0 + i of
-    // every quadrant), and the V scale factors of the chunk
-    {
+    // every quadrant), and the V scale bytes of token tid % 128
+    if (hf == 0) {
       uint32_t v0[4], v1[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -392,13 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st4(tmem_lane + kColSfb + buf * 8 + 4, v1[0], v1[1], v1[2], v1[3]);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     }
-    // token tid of the chunk: its 4 V scale bytes
-    const int vpi = tid >> 4, vtk = tid & 15;
+    const int vt = tid & (kChunk - 1);
+    const int vpi = vt >> 4, vtk = vt & 15;
     const bool vok = vpi < nv && (pg + vpi) * kPage + vtk < L;
     const uint32_t vsw = vok ? *reinterpret_cast<const uint32_t*>(smem + kOffVR + buf * kVR + vpi * kBlk +
                                                                   kCodeBytes + vtk * 4)
                              : 0u;
-    {
+    if (hf == 0) {
       uint32_t m4 = __vmaxu4(vsw, vsw >> 16);
       m4 = max(m4 & 0xFFu, (m4 >> 8) & 0xFFu);
       m4 = __reduce_max_sync(0xffffffffu, m4);
@@ -435,20 +445,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (groups more than 22 binades below E_x widen to zero: negligible values)
     const int e_x = max(e_c, e_ref - 30);
     // V factors 2^(e - E_x) as f16 (0 for tokens past the split or context)
+    if (hf == 0) {
 #pragma unroll
-    for (int g4 = 0; g4 < 4; ++g4) {
-      const int e = (int)((vsw >> (8 * g4)) & 0xFFu) - e_x;  // <= 0
-      const float f = (vok && e >= -126) ? __uint_as_float((uint32_t)(127 + e) << 23) : 0.0f;
-      fac[g4 * kChunk + tid] = __float2half_rn(f);
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const int e = (int)((vsw >> (8 * g4)) & 0xFFu) - e_x;  // <= 0
+        const float f = (vok && e >= -126) ? __uint_as_float((uint32_t)(127 + e) << 23) : 0.0f;
+        fac[g4 * kChunk + vt] = __float2half_rn(f);
+      }
     }
     __syncthreads();  // factors visible; P.V of the previous chunk was waited on
-    // ---- V' (dim tid, all 128 tokens of the chunk) -> canonical K-major tile
+    // ---- V' (dim tid % 128, pages 4h .. 4h + 3 of the chunk) -> canonical K-major tile
     {
-      const int d = tid, g4 = d >> 5;
+      const int d = tid & (D - 1), g4 = d >> 5;
       const uint8_t* vr = smem + kOffVR + buf * kVR + d * 8;
       const uint4* fr = reinterpret_cast<const uint4*>(fac + g4 * kChunk);
 #pragma unroll 2
-      for (int pi = 0; pi < kChunkPages; ++pi) {
+      for (int pp = 0; pp < kChunkPages / 2; ++pp) {
+        const int pi = hf * (kChunkPages / 2) + pp;
         const uint2 wv = *reinterpret_cast<const uint2*>(vr + pi * kBlk);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -467,23 +480,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!mbar_wait(sdone, (uint32_t)(c & 1))) timed_out = true;
     if (__any_sync(0xffffffffu, timed_out)) timed_out = true;
     fence_after_sync();
-    // the chunk's buffers are free once Q.K^T is done and V' is built: refill
-    // after the barrier below
     // tokens 0 .. nvr-1 of the chunk are visible to this row (the chunk's
     // positions are consecutive); whole warps with every token visible skip the
     // per-token test
     const int nvr = max(0, min(nv * kPage, my_limit - pg * kPage));
     const bool all_full = __all_sync(0xffffffffu, nvr == kChunk);
-    const uint32_t s_addr = tmem_lane + kColS;
+    const int lim0 = nvr - 64 * hf;  // visible tokens among this half's columns
     float cmx = -INFINITY;
     auto row_max = [&](auto masked) {
       constexpr bool M = decltype(masked)::value;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
         uint32_t sv[32];
         tmem_ld32(s_addr + 32 * q, sv);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        const int lim = nvr - 32 * q;
+        const int lim = lim0 - 32 * q;
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -497,6 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (all_full) row_max(std::false_type{});
       else row_max(std::true_type{});
     }
+    xch_s[hf][my_r] = cmx;
+    if (__syncthreads_or(timed_out)) {
+      timed_out = true;
+      break;
+    }
+    cmx = fmaxf(xch_s[0][my_r], xch_s[1][my_r]);
     const float m_new = cmx > m_run + 8.0f ? cmx : m_run;
     const float alpha = m_new == m_run ? 1.0f : ex2(m_run - m_new);
     m_run = m_new;
@@ -507,11 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto write_p = [&](auto masked) {
       constexpr bool M = decltype(masked)::value;
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t sv[32];
         tmem_ld32(s_addr + 32 * q, sv);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        const int lim = nvr - 32 * q;
+        const int lim = lim0 - 32 * q;
 #pragma unroll
         for (int o8 = 0; o8 < 4; ++o8) {
           uint32_t hw[4], lw[4];
@@ -526,49 +543,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p0 = ex2(x0 + shift), p1 = ex2(x1 + shift);
             ls4[i2] += p0 + p1;
             hw[i2] = pack_f16x2(p0, p1);
-            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[i2]));
-            lw[i2] = pack_f16x2(p0 - hf.x, p1 - hf.y);
+            const float2 hf2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[i2]));
+            lw[i2] = pack_f16x2(p0 - hf2.x, p1 - hf2.y);
           }
-          const int k8 = q * 4 + o8;  // token octet
+          const int k8 = hf * 8 + q * 4 + o8;  // token octet
           const int off = ((my_r >> 3) * 16 + k8) * 128 + (my_r & 7) * 16;
           *reinterpret_cast<uint4*>(smem + kOffP + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(smem + kOffP + kPF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
     };
-    if (!timed_out) {
-      if (all_full) write_p(std::false_type{});
-      else write_p(std::true_type{});
-    }
+    if (all_full) write_p(std::false_type{});
+    else write_p(std::true_type{});
     const float lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
     // l in the units of p (not p'): p = p' * 2^(E_ref - E_x), E_ref - E_x in [-4, 30]
-    l_run = l_run * alpha + lsum * __uint_as_float((uint32_t)(127 + e_ref - e_x) << 23);
-    // ---- fold the segment into the running O: at the end of a segment, and
-    // whenever the softmax or V reference moved (the fold applies the factor)
+    l_half = l_half * alpha + lsum * __uint_as_float((uint32_t)(127 + e_ref - e_x) << 23);
+    // ---- fold the segment into the running O (this half's dims): at the end
+    // of a segment, and whenever the softmax or V reference moved (the fold
+    // applies the factor)
     const float f_row = alpha * o_fac;
-    if (c > 0 && !timed_out && __any_sync(0xffffffffu, f_row != 1.0f || c % kFold == 0)) {
+    if (c > 0 && __any_sync(0xffffffffu, f_row != 1.0f || c % kFold == 0)) {
 #pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t ov[32], om[32];
-        tmem_ld32(tmem_lane + kColO + 32 * q, ov);
-        tmem_ld32(tmem_lane + kColOm + 32 * q, om);
+        tmem_ld32(tmem_lane + kColO + 64 * hf + 32 * q, ov);
+        tmem_ld32(tmem_lane + kColOm + 64 * hf + 32 * q, om);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           om[i] = __float_as_uint((__uint_as_float(om[i]) + __uint_as_float(ov[i])) * f_row);
           ov[i] = 0u;
         }
-        tmem_st32(tmem_lane + kColOm + 32 * q, om);
-        tmem_st32(tmem_lane + kColO + 32 * q, ov);
+        tmem_st32(tmem_lane + kColOm + 64 * hf + 32 * q, om);
+        tmem_st32(tmem_lane + kColO + 64 * hf + 32 * q, ov);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     }
     fence_proxy_async();  // P' and V' written by ordinary stores, read by the MMA
     fence_before_sync();
-    if (__syncthreads_or(timed_out)) {
-      timed_out = true;
-      break;
-    }
+    __syncthreads();
     fence_after_sync();
     // ---- P.V of the chunk; then refill the chunk's buffers with chunk c + 2
     if (tid == 0) {
@@ -607,18 +620,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_before_sync();
     __syncthreads();
   } else {
-    // ---- this split's output of row tid: O * 2^(E_ref - 127) / l (rotated
-    // space); the loads are warp-collective, rows past R only skip the stores
+    // ---- this split's output of row my_r, dims 64h .. 64h + 63:
+    // O * 2^(E_ref - 127) / l (rotated space); the loads are warp-collective,
+    // rows past R only skip the stores
+    xch_s[hf][my_r] = l_half;
+    __syncthreads();
+    const float l_row = xch_s[0][my_r] + xch_s[1][my_r];
     const bool valid_row = my_r < R;
     const size_t rr = valid_row ? row_index(my_r) * a.S + s : 0;
-    float* dst = a.part_o + rr * D;
-    const bool any = l_run > 0.0f;
-    const float sc = any ? __uint_as_float((uint32_t)e_ref << 23) / l_run : 0.0f;
+    float* dst = a.part_o + rr * D + 64 * hf;
+    const bool any = l_row > 0.0f;
+    const float sc = any ? __uint_as_float((uint32_t)e_ref << 23) / l_row : 0.0f;
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
       uint32_t ov[32], om[32];
-      tmem_ld32(tmem_lane + kColO + 32 * q, ov);
-      tmem_ld32(tmem_lane + kColOm + 32 * q, om);
+      tmem_ld32(tmem_lane + kColO + 64 * hf + 32 * q, ov);
+      tmem_ld32(tmem_lane + kColOm + 64 * hf + 32 * q, om);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       if (valid_row) {
 #pragma unroll
@@ -632,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (valid_row) a.part_lse[rr] = any ? (m_run + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    if (valid_row && hf == 0) a.part_lse[rr] = any ? (m_run + log2f(l_row)) * 0.69314718055994531f : -INFINITY;
     fence_before_sync();
     __syncthreads();
   }
