@@ -57,6 +57,10 @@ using namespace kv4::mma;
 constexpr int D = 128;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+// single threads that issue the MMAs and the copies: lane 0 of warps 7 and 6,
+// which have no scale-factor work in the chunk's serial part
+constexpr int kMmaThread = kThreads - 32;
+constexpr int kCopyThread = kThreads - 64;
 constexpr int kRows = 128;                            // query rows per CTA (MMA M)
 constexpr int kChunkPages = 8;
 constexpr int kChunk = kChunkPages * kPage;           // 128 tokens (Q.K^T N, P.V K)
@@ -251,11 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // chunk c -> buffer c & 1: four tensor gathers for K (codes, scales of 8
   // pages), two for V; pages past the split re-read the chunk's first page
   // (masked like tokens past the context).  Issued by thread 0.
-  auto issue = [&](int c) {
-    const int buf = c & 1;
+  auto load_rows = [&](int c, int (&rows)[kChunkPages]) {
     const int pg = p0 + c * kChunkPages;
     const int nv = min(kChunkPages, p1 - pg);
-    int rows[kChunkPages];
 #pragma unroll
     for (int i = 0; i < kChunkPages; ++i) {
       int page = 0;
@@ -268,6 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       rows[i] = i < nv ? page * a.Hkv + h : rows[0];
     }
+  };
+  auto issue = [&](int c, const int (&rows)[kChunkPages]) {
+    const int buf = c & 1;
     uint64_t* bar = &full[buf];
     mbar_expect_tx(bar, (uint32_t)(kChunkPages * (kCodeBytes + 64 + kBlk)));
 #pragma unroll
@@ -279,12 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_gather4(sbase + kOffVR + buf * kVR + q * 4 * kBlk, &maps.vblock, 0, r4[0], r4[1], r4[2], r4[3], bar);
     }
   };
-  // copies and MMAs issued (thread 0's counts) for the drain after a timeout
+  // copies (kCopyThread) and MMAs (kMmaThread) issued, for the drain after a
+  // timeout; the copy thread holds the page rows of chunk c + 2 from the start
+  // of iteration c, so their loads are long done when the copies go out
   int issued = 0, qk_issued = 0, pv_issued = 0;
-  if (tid == 0) {
+  int next_rows[kChunkPages];
+  if (tid == kCopyThread) {
     fence_proxy_async();
-    issue(0);
-    if (n_chunks > 1) issue(1);
+    load_rows(0, next_rows);
+    issue(0, next_rows);
+    if (n_chunks > 1) {
+      load_rows(1, next_rows);
+      issue(1, next_rows);
+    }
     issued = min(n_chunks, 2);
   }
 
@@ -385,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       break;
     }
     waited_full = c + 1;
+    if (tid == kCopyThread && c + 2 < n_chunks) load_rows(c + 2, next_rows);
     // ---- K scales into tensor memory (token 32i + lane at column c0 + i of
     // every quadrant), and the V scale bytes of token tid % 128
     if (hf == 0) {
@@ -418,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after_sync();
     // ---- Q.K^T of the chunk (one thread issues; the others go on to V)
-    if (tid == 0) {
+    if (tid == kMmaThread) {
       const uint32_t kb = sbase + kOffKC + buf * kKC;
 #pragma unroll
       for (int term = 0; term < kTerms; ++term)
@@ -453,9 +466,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         fac[g4 * kChunk + vt] = __float2half_rn(f);
       }
     }
-    __syncthreads();  // factors visible; P.V of the previous chunk was waited on
+    __syncthreads();  // factors visible
+    // V' and P' of the previous chunk are read by its P.V, which ran meanwhile
+    // (behind this chunk's Q.K^T on the tensor core)
+    if (c > 0) {
+      if (!mbar_wait(pvdone, (uint32_t)((c - 1) & 1))) timed_out = true;
+      fence_after_sync();
+    }
     // ---- V' (dim tid % 128, pages 4h .. 4h + 3 of the chunk) -> canonical K-major tile
-    {
+    if (!timed_out) {
       const int d = tid & (D - 1), g4 = d >> 5;
       const uint8_t* vr = smem + kOffVR + buf * kVR + d * 8;
       const uint4* fr = reinterpret_cast<const uint4*>(fac + g4 * kChunk);
@@ -520,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // p' = 2^(s - m + E_x - E_ref): the V factor folded into the exponent (a
     // row with nothing visible yet gets p' = 0)
     const float shift = m_new == -INFINITY ? -INFINITY : (float)(e_x - e_ref) - m_new;
-    float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const float2 sh2 = make_float2(shift, shift);
+    float2 ls2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
     auto write_p = [&](auto masked) {
       constexpr bool M = decltype(masked)::value;
 #pragma unroll 1
@@ -535,16 +555,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i2 = 0; i2 < 4; ++i2) {
             const int i = o8 * 8 + i2 * 2;
-            float x0 = __uint_as_float(sv[i]), x1 = __uint_as_float(sv[i + 1]);
+            float2 x = make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
             if (M) {
-              x0 = i < lim ? x0 : -INFINITY;
-              x1 = i + 1 < lim ? x1 : -INFINITY;
+              x.x = i < lim ? x.x : -INFINITY;
+              x.y = i + 1 < lim ? x.y : -INFINITY;
             }
-            const float p0 = ex2(x0 + shift), p1 = ex2(x1 + shift);
-            ls4[i2] += p0 + p1;
-            hw[i2] = pack_f16x2(p0, p1);
+            const float2 t = __fadd2_rn(x, sh2);
+            const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+            ls2[i2 & 1] = __fadd2_rn(ls2[i2 & 1], pp);
+            hw[i2] = pack_f16x2(pp.x, pp.y);
             const float2 hf2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[i2]));
-            lw[i2] = pack_f16x2(p0 - hf2.x, p1 - hf2.y);
+            const float2 lo = __fadd2_rn(pp, make_float2(-hf2.x, -hf2.y));
+            lw[i2] = pack_f16x2(lo.x, lo.y);
           }
           const int k8 = hf * 8 + q * 4 + o8;  // token octet
           const int off = ((my_r >> 3) * 16 + k8) * 128 + (my_r & 7) * 16;
@@ -555,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (all_full) write_p(std::false_type{});
     else write_p(std::true_type{});
-    const float lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+    const float lsum = (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
     // l in the units of p (not p'): p = p' * 2^(E_ref - E_x), E_ref - E_x in [-4, 30]
     l_half = l_half * alpha + lsum * __uint_as_float((uint32_t)(127 + e_ref - e_x) << 23);
     // ---- fold the segment into the running O (this half's dims): at the end
@@ -583,8 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // ---- P.V of the chunk; then refill the chunk's buffers with chunk c + 2
-    if (tid == 0) {
+    // ---- P.V of the chunk; the chunk's buffers are refilled with chunk c + 2
+    if (tid == kMmaThread) {
 #pragma unroll
       for (int ks = 0; ks < kChunk / 16; ++ks) {
         const uint64_t vd = smem_desc(sbase + kOffVF + ks * 256, 2048);
@@ -593,27 +615,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       commit(pvdone);
       ++pv_issued;
-      if (c + 2 < n_chunks) {
-        fence_proxy_async();
-        issue(c + 2);
-        issued = c + 3;
-      }
     }
-    // V' and P' are rewritten by the next chunk: wait for this P.V
-    if (!mbar_wait(pvdone, (uint32_t)(c & 1))) timed_out = true;
+    if (tid == kCopyThread && c + 2 < n_chunks) {
+      fence_proxy_async();
+      issue(c + 2, next_rows);
+      issued = c + 3;
+    }
+  }
+  // the last P.V
+  if (!timed_out) {
+    const bool ok = mbar_wait(pvdone, (uint32_t)((n_chunks - 1) & 1));
     fence_after_sync();
-    if (__syncthreads_or(timed_out)) {
-      timed_out = true;
-      break;
-    }
+    if (__syncthreads_or(!ok)) timed_out = true;
   }
 
   if (timed_out) {
     // Stop, but let every copy and MMA this CTA issued finish before the
     // shared and tensor memory are released (each wait again bounded).
-    if (tid == 0) {
+    if (tid == kCopyThread) {
       flag_error(a.dev_error, KV4_DEVERR_TIMEOUT);
       for (int c = waited_full; c < issued; ++c) (void)mbar_wait(&full[c & 1], (uint32_t)((c >> 1) & 1));
+    }
+    if (tid == kMmaThread) {
       if (qk_issued > 0) (void)mbar_wait(sdone, (uint32_t)((qk_issued - 1) & 1));
       if (pv_issued > 0) (void)mbar_wait(pvdone, (uint32_t)((pv_issued - 1) & 1));
     }
