@@ -31,10 +31,12 @@
 //          E_ref moves (and O is rescaled in tensor memory) only when a chunk's
 //          E_c exceeds it by more than 4, or with the softmax reference.
 //
-// One CTA per (split, position tile, kv head, sequence), 4 warps; 199 KB of
-// shared memory and 512 tensor-memory columns, so one CTA per SM.  The K and V
-// pages of chunk c + 2 stream in by tensor gathers while chunk c is processed.
-// Every wait is bounded; a timeout is agreed at a CTA barrier, flagged as
+// One CTA per (split, position tile, kv head, sequence), 8 warps; 216 KB of
+// shared memory and all 512 tensor-memory columns, so one CTA per SM.  The K
+// and V pages stream in by tensor gathers three chunks ahead.  The tensor core
+// runs the Q.K^T of chunk c + 1 (S is double-buffered in tensor memory) and the
+// P.V of chunk c - 1 while the CUDA cores widen V and run the softmax of chunk
+// c.  Every wait is bounded; a timeout is agreed at a CTA barrier, flagged as
 // KV4_DEVERR_TIMEOUT, and the kernel drains its copies and MMAs, frees its
 // tensor memory and returns.
 #include <cuda.h>
@@ -71,38 +73,41 @@ constexpr int kBlk = kCodeBytes + kPage * D / 32;     // 1088
 // shared memory map (bytes; operand tiles 128-byte aligned)
 constexpr int kQTerm = kRows * D / 2;                 // one q term: 128 rows x 64 B
 constexpr int kOffQ = 0;                              // [kTerms]
+constexpr int kRaw = 3;                               // chunk buffers: copies run 2 chunks ahead of Q.K^T
 constexpr int kKC = kChunkPages * kCodeBytes;         // K codes of a chunk
-constexpr int kOffKC = kOffQ + kTerms * kQTerm;       // [2 buffers]
+constexpr int kOffKC = kOffQ + kTerms * kQTerm;       // [kRaw]
 constexpr int kKS = kChunkPages * 64;                 // K scales of a chunk [8 pages][16 tokens][4]
-constexpr int kOffKS = kOffKC + 2 * kKC;              // [2 buffers]
+constexpr int kOffKS = kOffKC + kRaw * kKC;           // [kRaw]
 constexpr int kVR = kChunkPages * kBlk;               // V blocks of a chunk, as cached
-constexpr int kOffVR = kOffKS + 2 * kKS;              // [2 buffers]
+constexpr int kOffVR = kOffKS + kRaw * kKS;           // [kRaw]
 constexpr int kVF = D * kChunk * 2;                   // V' f16, 128 dims x 128 tokens
-constexpr int kOffVF = kOffVR + 2 * kVR;
+constexpr int kOffVF = kOffVR + kRaw * kVR;
 constexpr int kPF = kRows * kChunk * 2;               // P' f16, 128 rows x 128 tokens
 constexpr int kOffP = kOffVF + kVF;                   // [hi, lo]
 constexpr int kOffFac = kOffP + 2 * kPF;              // f16 [4 groups][128 tokens] V factors
 constexpr int kOffSfa = kOffFac + 4 * kChunk * 2;     // [kTerms][128 rows][4 groups] q scale bytes
 constexpr int kOffMisc = kOffSfa + kTerms * kRows * 4;  // [4] per-warp maxima
-constexpr int kOffBar = kOffMisc + 64;                // full[2], sdone, pvdone
-constexpr int kSmem = kOffBar + 8 * 4;
-static_assert(kOffKC % 1024 == 0 && kOffKS % 128 == 0 && kOffVR % 128 == 0 && (kOffVR + kVR) % 128 == 0 &&
+constexpr int kOffBar = kOffMisc + 64;                // full[kRaw], sdone[2], pvdone, drain
+constexpr int kNumBars = kRaw + 4;
+constexpr int kSmem = kOffBar + 8 * kNumBars;
+static_assert(kOffKC % 1024 == 0 && kOffKS % 128 == 0 && kOffVR % 128 == 0 && kVR % 128 == 0 &&
                   kOffVF % 128 == 0 && kOffP % 128 == 0 && kOffFac % 16 == 0 && kOffBar % 8 == 0,
               "operand and copy alignment");
 static_assert(kSmem <= 227 * 1024 && kSmem > 227 * 1024 / 2, "one CTA per SM (all 512 tensor-memory columns)");
 
 // tensor memory columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;      // S: 128 columns (tokens)
-constexpr uint32_t kColO = 128;    // O of the current segment of chunks: 128 columns (dims)
-constexpr uint32_t kColOm = 256;   // O of the segments before, summed by the CUDA cores
+constexpr uint32_t kColS = 0;      // S: [2 buffers][128 columns (tokens)]
+constexpr uint32_t kColO = 256;    // O of the current segment of chunks: 128 columns (dims)
 constexpr uint32_t kColSfa = 384;  // [kTerms][2 k-steps][4]
-constexpr uint32_t kColSfb = 472;  // [2 buffers][2 k-steps][4]
+constexpr uint32_t kColSfb = 448;  // [kRaw][2 k-steps][4]
+static_assert(kColSfa + kTerms * 8 <= kColSfb && kColSfb + kRaw * 8 <= kTmemCols, "tensor memory map");
 // The tensor core's own accumulation of O is kept to kFold chunks (kFold * 16
-// MMAs): a segment is then added into the running O by the CUDA cores (fp32,
-// round to nearest).  One accumulator over a 32K context (4096 MMAs) gave
-// sampled output errors up to 6e-4 and about 2e-3 over a whole step; with a
-// fold every 8 chunks they stay below 5e-5.
+// MMAs): a segment is then added into the running O, held in registers (64
+// values per thread), by the CUDA cores (fp32, round to nearest).  One
+// accumulator over a 32K context (4096 MMAs) gave sampled output errors up to
+// 6e-4 and about 2e-3 over a whole step; with a fold every 8 chunks they stay
+// below 5e-5.
 constexpr int kFold = 8;
 
 // kind::mxf4 (A = B = E2M1, UE8M0 scales), M = 128, N = 128; kind::f16 (f16
@@ -233,13 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t* table = a.block_tables + (size_t)b * a.max_pages;
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bars;        // [2]: one chunk's K codes, K scales and V blocks
-  uint64_t* sdone = bars + 2;   // Q.K^T of a chunk complete
-  uint64_t* pvdone = bars + 3;  // P.V of a chunk complete
+  uint64_t* full = bars;              // [kRaw]: one chunk's K codes, K scales and V blocks
+  uint64_t* sdone = bars + kRaw;      // [2]: Q.K^T into S buffer 0 / 1 complete
+  uint64_t* pvdone = bars + kRaw + 2; // P.V of a chunk complete
+  uint64_t* drain = bars + kRaw + 3;  // every MMA issued so far complete (after a timeout)
   int* wmax = reinterpret_cast<int*>(smem + kOffMisc);
 
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
   }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   if (w == 0) {
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_s;
   const uint32_t tmem_lane = tmem + ((uint32_t)(32 * qd) << 16);
 
-  // chunk c -> buffer c & 1: four tensor gathers for K (codes, scales of 8
+  // chunk c -> buffer c % kRaw: four tensor gathers for K (codes, scales of 8
   // pages), two for V; pages past the split re-read the chunk's first page
   // (masked like tokens past the context).  Issued by thread 0.
   auto load_rows = [&](int c, int (&rows)[kChunkPages]) {
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   auto issue = [&](int c, const int (&rows)[kChunkPages]) {
-    const int buf = c & 1;
+    const int buf = c % kRaw;
     uint64_t* bar = &full[buf];
     mbar_expect_tx(bar, (uint32_t)(kChunkPages * (kCodeBytes + 64 + kBlk)));
 #pragma unroll
@@ -286,19 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   // copies (kCopyThread) and MMAs (kMmaThread) issued, for the drain after a
-  // timeout; the copy thread holds the page rows of chunk c + 2 from the start
+  // timeout; the copy thread holds the page rows of chunk c + 3 from the start
   // of iteration c, so their loads are long done when the copies go out
-  int issued = 0, qk_issued = 0, pv_issued = 0;
+  int issued = 0, qk_issued = 0;
   int next_rows[kChunkPages];
   if (tid == kCopyThread) {
     fence_proxy_async();
-    load_rows(0, next_rows);
-    issue(0, next_rows);
-    if (n_chunks > 1) {
-      load_rows(1, next_rows);
-      issue(1, next_rows);
+    for (int c = 0; c < min(n_chunks, kRaw); ++c) {
+      load_rows(c, next_rows);
+      issue(c, next_rows);
     }
-    issued = min(n_chunks, 2);
+    issued = min(n_chunks, kRaw);
   }
 
   // ---- q prologue: rotate (fp32 butterfly), times softmax_scale*log2e/sqrt(D),
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // q scale factors into tensor memory, replicated in every lane quadrant:
   // column c0 + i of lane l holds row 32i + l (the MMA reads row m at lane m,
-  // column c0 + m/32).  The running O starts at zero.
+  // column c0 + m/32).
   if (hf == 0) {
 #pragma unroll 1
     for (int term = 0; term < kTerms; ++term)
@@ -364,15 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st4(tmem_lane + kColSfa + (term * 2 + ks) * 4, v[0], v[1], v[2], v[3]);
       }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   }
-  {
-    uint32_t z[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll
-    for (int q = 0; q < 2; ++q) tmem_st32(tmem_lane + kColOm + 64 * hf + 32 * q, z);
-  }
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   fence_proxy_async();  // q terms written by ordinary stores, read by the MMA
 
   // this thread's row and column half
@@ -380,46 +377,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int my_limit = my_r < R ? L - Tc + 1 + my_r / G : 0;
   float m_run = -INFINITY;
   float l_half = 0.0f;  // this half's share of the row sum
+  float om[64];         // running O of this row's half, summed segments
+#pragma unroll
+  for (int i = 0; i < 64; ++i) om[i] = 0.0f;
   int e_ref = 0;        // V scale reference (UE8M0 byte value)
   bool timed_out = false;
   int waited_full = 0;
   __half* fac = reinterpret_cast<__half*>(smem + kOffFac);  // [4][128]
-  const uint32_t s_addr = tmem_lane + kColS + 64 * hf;
 
-#pragma unroll 1
-  for (int c = 0; c < n_chunks; ++c) {
-    const int buf = c & 1;
+  // Wait for chunk c's pages; the warps of half 0 write its K scales into
+  // tensor memory (token 32i + lane at column c0 + i of every quadrant).
+  auto stage_k = [&](int c) {
+    const int rb = c % kRaw;
     const int pg = p0 + c * kChunkPages;
     const int nv = min(kChunkPages, p1 - pg);
-    // ---- wait for the chunk's pages
-    if (!mbar_wait(&full[buf], (uint32_t)((c >> 1) & 1))) timed_out = true;
-    if (__syncthreads_or(timed_out)) {
-      timed_out = true;
-      break;
-    }
-    waited_full = c + 1;
-    if (tid == kCopyThread && c + 2 < n_chunks) load_rows(c + 2, next_rows);
-    // ---- K scales into tensor memory (token 32i + lane at column c0 + i of
-    // every quadrant), and the V scale bytes of token tid % 128
-    if (hf == 0) {
+    if (!mbar_wait(&full[rb], (uint32_t)((c / kRaw) & 1))) timed_out = true;
+    if (hf == 0 && __all_sync(0xffffffffu, !timed_out)) {
       uint32_t v0[4], v1[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int n = 32 * i + lane, pi = n >> 4, tk = n & 15;
         const bool ok = pi < nv && (pg + pi) * kPage + tk < L;
-        const uint32_t sw = ok ? *reinterpret_cast<const uint32_t*>(smem + kOffKS + buf * kKS + pi * 64 + tk * 4)
+        const uint32_t sw = ok ? *reinterpret_cast<const uint32_t*>(smem + kOffKS + rb * kKS + pi * 64 + tk * 4)
                                : 0x7F7F7F7Fu;
         v0[i] = (sw & 0xFFFFu) | 0x7F7F0000u;
         v1[i] = (sw >> 16) | 0x7F7F0000u;
       }
-      tmem_st4(tmem_lane + kColSfb + buf * 8 + 0, v0[0], v0[1], v0[2], v0[3]);
-      tmem_st4(tmem_lane + kColSfb + buf * 8 + 4, v1[0], v1[1], v1[2], v1[3]);
+      tmem_st4(tmem_lane + kColSfb + rb * 8 + 0, v0[0], v0[1], v0[2], v0[3]);
+      tmem_st4(tmem_lane + kColSfb + rb * 8 + 4, v1[0], v1[1], v1[2], v1[3]);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     }
+  };
+  // Q.K^T of chunk c into S buffer c & 1 (one thread, after a CTA barrier)
+  auto issue_qk = [&](int c) {
+    const int rb = c % kRaw;
+    const uint32_t kb = sbase + kOffKC + rb * kKC;
+#pragma unroll
+    for (int term = 0; term < kTerms; ++term)
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+        mma_mxf4(tmem + kColS + (c & 1) * kChunk, smem_desc(sbase + kOffQ + term * kQTerm + ks * 256, 512),
+                 smem_desc(kb + ks * 256, 512), tmem + kColSfa + (term * 2 + ks) * 4,
+                 tmem + kColSfb + rb * 8 + ks * 4, (term | ks) != 0);
+    commit(&sdone[c & 1]);
+    ++qk_issued;
+  };
+
+  // chunk 0's Q.K^T goes out before the loop; inside, chunk c + 1's is issued
+  // before chunk c's softmax, so the tensor core works while the CUDA cores do
+  stage_k(0);
+  fence_before_sync();
+  if (__syncthreads_or(timed_out)) timed_out = true;
+  fence_after_sync();
+  waited_full = 1;
+  if (!timed_out && tid == kMmaThread) issue_qk(0);
+
+#pragma unroll 1
+  for (int c = 0; c < n_chunks && !timed_out; ++c) {
+    const int rb = c % kRaw;
+    const int pg = p0 + c * kChunkPages;
+    const int nv = min(kChunkPages, p1 - pg);
+    // ---- next chunk's K; this chunk's V scale bytes (token tid % 128)
+    if (c + 1 < n_chunks) stage_k(c + 1);
+    if (tid == kCopyThread && c + kRaw < n_chunks) load_rows(c + kRaw, next_rows);
     const int vt = tid & (kChunk - 1);
     const int vpi = vt >> 4, vtk = vt & 15;
     const bool vok = vpi < nv && (pg + vpi) * kPage + vtk < L;
-    const uint32_t vsw = vok ? *reinterpret_cast<const uint32_t*>(smem + kOffVR + buf * kVR + vpi * kBlk +
+    const uint32_t vsw = vok ? *reinterpret_cast<const uint32_t*>(smem + kOffVR + rb * kVR + vpi * kBlk +
                                                                   kCodeBytes + vtk * 4)
                              : 0u;
     if (hf == 0) {
@@ -429,21 +453,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) wmax[w] = (int)m4;
     }
     fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    // ---- Q.K^T of the chunk (one thread issues; the others go on to V)
-    if (tid == kMmaThread) {
-      const uint32_t kb = sbase + kOffKC + buf * kKC;
-#pragma unroll
-      for (int term = 0; term < kTerms; ++term)
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          mma_mxf4(tmem + kColS, smem_desc(sbase + kOffQ + term * kQTerm + ks * 256, 512),
-                   smem_desc(kb + ks * 256, 512), tmem + kColSfa + (term * 2 + ks) * 4,
-                   tmem + kColSfb + buf * 8 + ks * 4, (term | ks) != 0);
-      commit(sdone);
-      ++qk_issued;
+    if (__syncthreads_or(timed_out)) {
+      timed_out = true;
+      break;
     }
+    fence_after_sync();
+    waited_full = min(n_chunks, c + 2);
+    if (tid == kMmaThread && c + 1 < n_chunks) issue_qk(c + 1);
     const int e_c = max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3]));
     // V reference: set by the first chunk, raised when a chunk exceeds it by > 4
     float o_fac = 1.0f;
@@ -469,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();  // factors visible
     // V' and P' of the previous chunk are read by its P.V, which ran meanwhile
-    // (behind this chunk's Q.K^T on the tensor core)
     if (c > 0) {
       if (!mbar_wait(pvdone, (uint32_t)((c - 1) & 1))) timed_out = true;
       fence_after_sync();
@@ -477,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- V' (dim tid % 128, pages 4h .. 4h + 3 of the chunk) -> canonical K-major tile
     if (!timed_out) {
       const int d = tid & (D - 1), g4 = d >> 5;
-      const uint8_t* vr = smem + kOffVR + buf * kVR + d * 8;
+      const uint8_t* vr = smem + kOffVR + rb * kVR + d * 8;
       const uint4* fr = reinterpret_cast<const uint4*>(fac + g4 * kChunk);
 #pragma unroll 2
       for (int pp = 0; pp < kChunkPages / 2; ++pp) {
@@ -497,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---- S of the chunk
-    if (!mbar_wait(sdone, (uint32_t)(c & 1))) timed_out = true;
+    if (!mbar_wait(&sdone[c & 1], (uint32_t)((c >> 1) & 1))) timed_out = true;
     if (__any_sync(0xffffffffu, timed_out)) timed_out = true;
     fence_after_sync();
     // tokens 0 .. nvr-1 of the chunk are visible to this row (the chunk's
@@ -506,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nvr = max(0, min(nv * kPage, my_limit - pg * kPage));
     const bool all_full = __all_sync(0xffffffffu, nvr == kChunk);
     const int lim0 = nvr - 64 * hf;  // visible tokens among this half's columns
+    const uint32_t s_addr = tmem_lane + kColS + (c & 1) * kChunk + 64 * hf;
     float cmx = -INFINITY;
     auto row_max = [&](auto masked) {
       constexpr bool M = decltype(masked)::value;
@@ -586,18 +602,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // applies the factor)
     const float f_row = alpha * o_fac;
     if (c > 0 && __any_sync(0xffffffffu, f_row != 1.0f || c % kFold == 0)) {
-#pragma unroll 1
+#pragma unroll
       for (int q = 0; q < 2; ++q) {
-        uint32_t ov[32], om[32];
+        uint32_t ov[32];
         tmem_ld32(tmem_lane + kColO + 64 * hf + 32 * q, ov);
-        tmem_ld32(tmem_lane + kColOm + 64 * hf + 32 * q, om);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          om[i] = __float_as_uint((__uint_as_float(om[i]) + __uint_as_float(ov[i])) * f_row);
+          om[32 * q + i] = (om[32 * q + i] + __uint_as_float(ov[i])) * f_row;
           ov[i] = 0u;
         }
-        tmem_st32(tmem_lane + kColOm + 64 * hf + 32 * q, om);
         tmem_st32(tmem_lane + kColO + 64 * hf + 32 * q, ov);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -606,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // ---- P.V of the chunk; the chunk's buffers are refilled with chunk c + 2
+    // ---- P.V of the chunk; the chunk's buffers are refilled with chunk c + kRaw
     if (tid == kMmaThread) {
 #pragma unroll
       for (int ks = 0; ks < kChunk / 16; ++ks) {
@@ -615,12 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_f16(tmem + kColO, smem_desc(sbase + kOffP + kPF + ks * 256, 2048), vd, 1);
       }
       commit(pvdone);
-      ++pv_issued;
     }
-    if (tid == kCopyThread && c + 2 < n_chunks) {
+    if (tid == kCopyThread && c + kRaw < n_chunks) {
       fence_proxy_async();
-      issue(c + 2, next_rows);
-      issued = c + 3;
+      issue(c + kRaw, next_rows);
+      issued = c + kRaw + 1;
     }
   }
   // the last P.V
@@ -632,14 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (timed_out) {
     // Stop, but let every copy and MMA this CTA issued finish before the
-    // shared and tensor memory are released (each wait again bounded).
+    // shared and tensor memory are released (each wait again bounded): the
+    // copies by their own barriers, the MMAs by one more commit.
     if (tid == kCopyThread) {
       flag_error(a.dev_error, KV4_DEVERR_TIMEOUT);
-      for (int c = waited_full; c < issued; ++c) (void)mbar_wait(&full[c & 1], (uint32_t)((c >> 1) & 1));
+      for (int c = waited_full; c < issued; ++c) (void)mbar_wait(&full[c % kRaw], (uint32_t)((c / kRaw) & 1));
     }
-    if (tid == kMmaThread) {
-      if (qk_issued > 0) (void)mbar_wait(sdone, (uint32_t)((qk_issued - 1) & 1));
-      if (pv_issued > 0) (void)mbar_wait(pvdone, (uint32_t)((pv_issued - 1) & 1));
+    if (tid == kMmaThread && qk_issued > 0) {
+      commit(drain);
+      (void)mbar_wait(drain, 0u);
     }
     fence_before_sync();
     __syncthreads();
@@ -655,20 +669,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* dst = a.part_o + rr * D + 64 * hf;
     const bool any = l_row > 0.0f;
     const float sc = any ? __uint_as_float((uint32_t)e_ref << 23) / l_row : 0.0f;
-#pragma unroll 1
+#pragma unroll
     for (int q = 0; q < 2; ++q) {
-      uint32_t ov[32], om[32];
+      uint32_t ov[32];
       tmem_ld32(tmem_lane + kColO + 64 * hf + 32 * q, ov);
-      tmem_ld32(tmem_lane + kColOm + 64 * hf + 32 * q, om);
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       if (valid_row) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           float4 o4;
-          o4.x = (__uint_as_float(om[i]) + __uint_as_float(ov[i])) * sc;
-          o4.y = (__uint_as_float(om[i + 1]) + __uint_as_float(ov[i + 1])) * sc;
-          o4.z = (__uint_as_float(om[i + 2]) + __uint_as_float(ov[i + 2])) * sc;
-          o4.w = (__uint_as_float(om[i + 3]) + __uint_as_float(ov[i + 3])) * sc;
+          o4.x = (om[32 * q + i] + __uint_as_float(ov[i])) * sc;
+          o4.y = (om[32 * q + i + 1] + __uint_as_float(ov[i + 1])) * sc;
+          o4.z = (om[32 * q + i + 2] + __uint_as_float(ov[i + 2])) * sc;
+          o4.w = (om[32 * q + i + 3] + __uint_as_float(ov[i + 3])) * sc;
           *reinterpret_cast<float4*>(dst + 32 * q + i) = o4;
         }
       }
