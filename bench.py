@@ -44,6 +44,7 @@ from bit_kv_cache_rotate_b300 import workloads as W  # noqa: E402
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 DECODE_SOURCES = ("bit_kv_cache_rotate_b300/csrc/kv4_decode_mma.cu",
+                  "bit_kv_cache_rotate_b300/csrc/kv4_extend_tc.cu",
                   "bit_kv_cache_rotate_b300/csrc/kv4_mma_common.cuh",
                   "bit_kv_cache_rotate_b300/csrc/kv4_decode.h")
 METRIC = "4-bit-KV decode attention: HBM GB/s (% of peak) and ms/step at 32K ctx, batch 32"
@@ -383,7 +384,7 @@ def run_ours(args, rank, world, local_rank):
         metric, unit = EXTEND_METRIC, "TFLOP/s"
         value = flops * world / (ms_per_step * 1e-3) / 1e12
         e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "kv4 decode split kernel (query positions tiled over CTAs)",
+        roofline = {"bound": "tensor", "kernel": "kv4 extend kernel (tcgen05: mxf4 Q.K^T, f16 P.V)",
                     "achieved": round(achieved, 1), "peak": peak,
                     "peak_kind": f"{peak_kind} (dense bf16 GEMM, burst; f16 MMAs run at the bf16 rate)",
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": stored_traffic(cfg.name),

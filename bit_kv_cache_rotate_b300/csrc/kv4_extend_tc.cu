@@ -592,8 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    if (all_full) write_p(std::false_type{});
-    else write_p(std::true_type{});
+    if (!timed_out) {
+      if (all_full) write_p(std::false_type{});
+      else write_p(std::true_type{});
+    }
     const float lsum = (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
     // l in the units of p (not p'): p = p' * 2^(E_ref - E_x), E_ref - E_x in [-4, 30]
     l_half = l_half * alpha + lsum * __uint_as_float((uint32_t)(127 + e_ref - e_x) << 23);
@@ -601,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of a segment, and whenever the softmax or V reference moved (the fold
     // applies the factor)
     const float f_row = alpha * o_fac;
-    if (c > 0 && __any_sync(0xffffffffu, f_row != 1.0f || c % kFold == 0)) {
+    if (c > 0 && !timed_out && __any_sync(0xffffffffu, f_row != 1.0f || c % kFold == 0)) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t ov[32];
@@ -618,7 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_proxy_async();  // P' and V' written by ordinary stores, read by the MMA
     fence_before_sync();
-    __syncthreads();
+    if (__syncthreads_or(timed_out)) {
+      timed_out = true;
+      break;
+    }
     fence_after_sync();
     // ---- P.V of the chunk; the chunk's buffers are refilled with chunk c + kRaw
     if (tid == kMmaThread) {
