@@ -97,11 +97,15 @@ __global__ void __launch_bounds__(kRefThreads) decode_ref_kernel(DecodeArgs a) {
     }
     const uint8_t* kb = a.k_cache + ((size_t)page * a.Hkv + h) * BLK;
     const uint8_t* vb = a.v_cache + ((size_t)page * a.Hkv + h) * BLK;
-    // ---- decode the page to fp32 (rotated space for the 4-bit cache)
+    // ---- decode the page to fp32 (rotated space for the 4-bit cache).
+    // Slots past the context were never written and may hold any bytes (a
+    // UE8M0 0xFF is 2^128, an E4M3 0xFF a NaN); their values are taken as 0,
+    // since a zero softmax weight times an infinite or NaN value is NaN.
     for (int idx = tid; idx < kPage * D; idx += kRefThreads) {
       const int t = idx / D, d = idx % D;
-      float kv, vv;
-      if constexpr (FP8) {
+      float kv = 0.0f, vv = 0.0f;
+      if (bad || p * kPage + t >= L) {
+      } else if constexpr (FP8) {
         kv = e4m3x2_to_f32x2(kb[t * D + d]).x * ksc;
         vv = e4m3x2_to_f32x2(vb[d * kPage + t]).x * vsc;
       } else {
