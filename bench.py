@@ -45,6 +45,7 @@ FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 DECODE_SOURCES = ("bit_kv_cache_rotate_b300/csrc/kv4_decode_mma.cu",
                   "bit_kv_cache_rotate_b300/csrc/kv4_extend_tc.cu",
+                  "bit_kv_cache_rotate_b300/csrc/kv4_decode_mla.cu",
                   "bit_kv_cache_rotate_b300/csrc/kv4_mma_common.cuh",
                   "bit_kv_cache_rotate_b300/csrc/kv4_decode.h")
 METRIC = "4-bit-KV decode attention: HBM GB/s (% of peak) and ms/step at 32K ctx, batch 32"

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
   // the first read are mostly served by L2.
   const int n_tiles = a.pos_split ? (a.T + a.pos_tile - 1) / a.pos_tile : 1;
   const int s = (int)blockIdx.x / n_tiles;
-  const int h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.y, b = mma::longest_first(a.context_lens, a.B, blockIdx.z);
   const int j0 = a.pos_split ? ((int)blockIdx.x % n_tiles) * a.pos_tile : 0;
   const int Tc = a.pos_split ? min(a.pos_tile, a.T - j0) : a.T;  // query positions in this CTA
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;

@@ -127,5 +127,32 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t word, int half) {
   return out;
 }
 
+// Sequence served by grid row z.  CTAs start roughly in launch order (x
+// fastest, then y, then z), and with ragged contexts a sequence's CTAs take
+// time in proportion to its length; so row z takes the z-th longest sequence
+// (ties by index), the long sequences start in the first wave and the short
+// ones fill the tail of the last.  Equal lengths give z itself.  Each warp
+// ranks the lengths on its own (lane i holds sequences i and i + 32): no
+// shared memory, no block barrier; every lane of a full warp must call it.
+// Batches above kOrderMaxBatch keep the launch order.
+constexpr int kOrderMaxBatch = 64;
+
+__device__ __forceinline__ int longest_first(const int32_t* __restrict__ lens, int B, int z) {
+  if (B > kOrderMaxBatch) return z;
+  const int lane = threadIdx.x & 31;
+  const int i1 = lane + 32;
+  const int L0 = lane < B ? lens[lane] : 0;
+  const int L1 = i1 < B ? lens[i1] : 0;
+  int r0 = 0, r1 = 0;
+  for (int j = 0; j < B; ++j) {
+    const int Lj = __shfl_sync(0xffffffffu, j < 32 ? L0 : L1, j & 31);
+    r0 += (Lj > L0) | ((Lj == L0) & (j < lane));
+    r1 += (Lj > L1) | ((Lj == L1) & (j < i1));
+  }
+  const uint32_t m0 = __ballot_sync(0xffffffffu, lane < B && r0 == z);
+  const uint32_t m1 = __ballot_sync(0xffffffffu, i1 < B && r1 == z);
+  return m0 ? __ffs(m0) - 1 : (m1 ? 31 + __ffs(m1) : z);
+}
+
 }  // namespace mma
 }  // namespace kv4
