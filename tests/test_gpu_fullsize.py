@@ -4,7 +4,7 @@ decode with the automatic split count) runs on the GPU; sampled (sequence, kv
 head) pairs are recomputed one by one by the oracle -- every cached K/V block
 of the sample bit-exact, its attention rows within 2e-3.  Workloads covered:
 batch 32 at a 32K context (4-bit path and the FP8 comparator on the same
-inputs), the 512-wide MLA latent cache at batch 8 and a 96K context, the
+inputs) and at 8K, the 512-wide MLA latent cache at batch 8 and a 96K context, the
 3-position verify step over ragged 16K-128K contexts with a 93 % shared prefix,
 and the extend step (batch 4, a 512-token chunk over a 32K context) on both
 extend kernels at sampled chunk positions."""
@@ -153,6 +153,18 @@ def _bench_step(name):
                                    cfg.softmax_scale, num_splits=wl.S, workspace_buf=wl.ws)
     torch.cuda.synchronize()
     return cfg, wl, out.cpu().numpy().astype(np.float64)
+
+
+# ---- batch 32 at an 8K context (the same kernel, a quarter of the tokens per split)
+@pytest.fixture(scope="module")
+def fullsize_8k():
+    return _bench_step("b32_ctx8k")
+
+
+@pytest.mark.parametrize("b,h", [(5, 1), (30, 7)])
+def test_fullsize_8k_sampled_parity(fullsize_8k, b, h):
+    cfg, wl, out = fullsize_8k
+    _check_sample(cfg, wl, out, b, h)
 
 
 # ---- MLA latent cache at full size: batch 8, a 98304-token context, one 512-wide latent head
