@@ -32,7 +32,8 @@ PAGE_SIZE = 16
 
 EXPORTS = ("kv4_status_string", "kv4_cache_bytes", "kv4_append_quantize", "kv4_decode_auto_splits",
            "kv4_decode_workspace_bytes", "kv4_decode_attention", "kv4_decode_partials", "kv4_split_combine",
-           "fp8_cache_bytes", "fp8_append_quantize", "fp8_decode_attention")
+           "fp8_cache_bytes", "fp8_append_quantize", "fp8_decode_attention",
+           "kv4_decode_attention_noalloc")
 
 
 class Kv4Error(RuntimeError):
@@ -71,6 +72,9 @@ def _load() -> ctypes.CDLL:
     L.fp8_decode_attention.restype = i32
     L.kv4_split_combine.argtypes = [P, P, i32, i32, i32, i32, i32, P, P]
     L.kv4_split_combine.restype = i32
+    L.kv4_decode_attention_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
+                                               i32, P, P, P]
+    L.kv4_decode_attention_noalloc.restype = i32
     return L
 
 
@@ -228,13 +232,10 @@ def kv4_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens
     B, T, Hq, D = q.shape
     if out is None:
         out = torch.empty((B, T, Hq, D), dtype=torch.float32, device=q.device)
-    fn = lib().kv4_decode_attention_noalloc
-    P, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-    fn.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, P, P, P]
-    fn.restype = i32
-    st = fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), B, T, Hq,
-            num_kv_heads, D, page_size, block_tables.shape[1], num_pages, float(softmax_scale), num_splits,
-            _ptr(out), _ptr(dev_error), _stream(stream))
+    st = lib().kv4_decode_attention_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                            _ptr(context_lens), B, T, Hq, num_kv_heads, D, page_size,
+                                            block_tables.shape[1], num_pages, float(softmax_scale), num_splits,
+                                            _ptr(out), _ptr(dev_error), _stream(stream))
     _check("kv4_decode_attention_noalloc", st)
     return out
 
