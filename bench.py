@@ -344,6 +344,29 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_s) + ((h_v,) if h_v is not None else ()))
     d2h = h_out.numel() * h_out.element_size()
 
+    # ---- the step's append and combine alone: each launch repeated in a graph of
+    # its own (idempotent: the same tokens land in the same slots), so the
+    # step's own timing carries no extra event nodes
+    def timed_graph(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        del g
+        return a.elapsed_time(b) / n
+
+    n_parts = max(1, min(args.steps, 200))
+    append_ms = timed_graph(lambda: kv4.kv4_append_quantize(wl.new_k, wl.new_v, wl.new_slots, wl.kc, wl.vc,
+                                                            lay.num_pages), n_parts)
+    combine_ms = timed_graph(lambda: kv4.kv4_split_combine(po, pl, out=wl.out), n_parts)
+
     # ---- FP8 comparator on identical inputs
     fp8_info = None
     if wl.fp8 is not None:
@@ -423,6 +446,11 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 1), "unit": unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
+        "step_parts_ms": {"append": round(append_ms, 5), "decode_split": round(kern_ms, 5),
+                          "combine": round(combine_ms, 5),
+                          "note": f"append quantises the step's {cfg.batch * cfg.q_per_seq} new tokens x "
+                                  f"{cfg.num_kv_heads} kv heads; append and combine timed alone, "
+                                  f"{n_parts} launches in a CUDA graph"},
         "clocks": clk.summary(),
     }
     if fp8_info:
