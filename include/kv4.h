@@ -32,7 +32,11 @@
  *     (4-bit cache without the latent mode, and the FP8 cache); every other
  *     shape takes R up to 64 (32 at head_dim 256, 16 at 512) and returns
  *     KV4_ERR_UNSUPPORTED above that.
- *   - Entry points hold no global state and are thread-safe.
+ *   - Entry points are thread-safe.  Their only process-wide state is set up
+ *     once and never changes results: each kernel's raised shared-memory
+ *     limit (per device), the driver's tensor-map encoder (looked up once),
+ *     and for kv4_decode_attention_noalloc the address of its scratch array
+ *     (per device; that array's ordering rule is stated there).
  *
  * Cache layout (one block per (page, kv head), blocks page-major:
  * block index = page * num_kv_heads + head, block bytes = P*D/2 + P*D/32):
