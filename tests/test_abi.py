@@ -90,3 +90,57 @@ def test_host_validation_rejects_before_launch(lib):
 def test_status_strings(lib):
     for s in range(5):
         assert lib.kv4_status_string(s)
+
+
+def test_more_host_validation(lib):
+    """Each of these returns before any launch or CUDA call."""
+    P = ctypes.c_void_p
+    fake = P(4096)
+    ws = P(4096 * 256)
+    dec = lib.kv4_decode_attention
+
+    def args(q=fake, B=2, T=1, Hq=8, Hkv=2, D=128, S=1, ws_ptr=ws, ws_bytes=1 << 24, out=fake):
+        return [q, fake, fake, fake, fake, B, T, Hq, Hkv, D, 16, 4, 8, 0.1, S, ws_ptr, ws_bytes, out, None, None]
+
+    assert dec(*args(S=-1)) == kv4.KV4_ERR_INVALID_ARG
+    assert dec(*args(S=4097)) == kv4.KV4_ERR_INVALID_ARG
+    assert dec(*args(q=P(4098))) == kv4.KV4_ERR_INVALID_ARG          # q not 16-byte aligned
+    assert dec(*args(ws_ptr=P(4096 * 256 + 128))) == kv4.KV4_ERR_INVALID_ARG  # workspace not 256-byte aligned
+    assert dec(*args(out=P(4100))) == kv4.KV4_ERR_INVALID_ARG        # out not 16-byte aligned
+    assert dec(*args(out=None)) == kv4.KV4_ERR_INVALID_ARG
+    assert dec(*args(Hkv=0)) == kv4.KV4_ERR_INVALID_ARG
+    # the general kernel's row limits: 64 rows at head_dim 64, 16 for the 512-wide latent cache
+    assert dec(*args(D=64, T=9, Hq=16, Hkv=2)) == kv4.KV4_ERR_UNSUPPORTED
+    lat = args(D=512, T=2, Hq=16, Hkv=1)
+    lat[2] = None  # latent cache: no separate V
+    assert dec(*lat) == kv4.KV4_ERR_UNSUPPORTED
+    # the split stage alone needs an explicit split count
+    part = args()
+    del part[17]  # kv4_decode_partials has no output argument
+    part[14] = 0
+    assert lib.kv4_decode_partials(*part) == kv4.KV4_ERR_INVALID_ARG
+    # FP8 decode needs both per-head scales
+    f8 = lib.fp8_decode_attention
+    f8_args = lambda ks, vs: [fake, fake, fake, ks, vs, fake, fake, 2, 1, 8, 2, 128, 16, 4, 8, 0.1, 1, ws, 1 << 24,
+                              fake, None, None]
+    assert f8(*f8_args(None, fake)) == kv4.KV4_ERR_INVALID_ARG
+    assert f8(*f8_args(fake, None)) == kv4.KV4_ERR_INVALID_ARG
+    # FP8 append: misaligned bf16 input
+    assert lib.fp8_append_quantize(P(4100), fake, 4, 8, 128, fake, fake, fake, fake, fake, 10, 16, None, None) == \
+        kv4.KV4_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_before_touching_the_device(lib):
+    """An explicit split count whose partials exceed the fixed scratch, or a
+    negative one, is refused before the scratch address is looked up."""
+    P = ctypes.c_void_p
+    fake = P(4096)
+    na = lib.kv4_decode_attention_noalloc
+    B, T, Hq, Hkv, D = 64, 1, 64, 8, 128
+    need = kv4.kv4_decode_workspace_bytes(B, T, Hq, D, 64)
+    assert need > (16 << 20)
+    assert na(fake, fake, fake, fake, fake, B, T, Hq, Hkv, D, 16, 4, 8, 0.1, 64, fake, None, None) == \
+        kv4.KV4_ERR_INVALID_ARG
+    assert na(fake, fake, fake, fake, fake, B, T, Hq, Hkv, D, 16, 4, 8, 0.1, -1, fake, None, None) == \
+        kv4.KV4_ERR_INVALID_ARG
+    assert na(fake, fake, fake, fake, fake, 0, T, Hq, Hkv, D, 16, 4, 8, 0.1, 0, fake, None, None) == kv4.KV4_OK
