@@ -65,7 +65,9 @@ __global__ void __launch_bounds__(256) append_fp4_kernel(
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    y[i] = (float)(x[i] * inv_sqrt_d);
+    // + 0.0 turns an exact zero sum into +0: a butterfly over negative zeros
+    // yields -0 where the exact matrix product has a plain 0 (code 0, not 8).
+    y[i] = (float)(x[i] * inv_sqrt_d + 0.0);
     amax = fmaxf(amax, fabsf(y[i]));
   }
 #pragma unroll

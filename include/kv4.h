@@ -106,7 +106,8 @@ size_t kv4_cache_bytes(int num_pages, int num_kv_heads, int page_size, int head_
  * Per (token, head): y = fp32(fp64(exact(H+-1 . x)) * RN64(1/sqrt(D))); per
  * 32-channel group e = clamp(floor(log2 max|y|) - 2, -127, 127) (e = -127 for
  * an all-zero group); code = RNE_E2M1_saturating(y / 2^e) with the sign bit
- * kept for values that round to zero; the scale byte is e + 127.
+ * kept for nonzero values that round to zero (an exact zero y is +0); the
+ * scale byte is e + 127.
  * Codes and scales are bit-exact for vectors whose exact Hadamard sum is
  * representable in binary64 (in-vector dynamic range below about 2^40).
  * Concurrent appends to the two tokens sharing a V byte are safe. */
