@@ -496,21 +496,36 @@ def oracle_sample(cfg, lay, n_seqs: int, head=None):
     return step, nbytes
 
 
-def cpu_baseline(cfg, lay, budget_s: float = 12.0):
+def cpu_baseline(cfg, lay, budget_s: float = 12.0, single_budget_s: float = 4.0):
+    """The oracle on one sequence of the workload (all kv heads): its OpenMP loop
+    runs over the sequence's (sequence, kv head) pairs, so it uses at most that
+    many host threads; a single-thread figure is timed beside it."""
+    import oracle
     step, nbytes = oracle_sample(cfg, lay, 1)
-    threads = min(os.cpu_count() or 1, cfg.num_kv_heads)
-    os.environ.setdefault("OMP_NUM_THREADS", str(threads))
-    n, t0 = 0, time.perf_counter()
-    while True:
-        step()
-        n += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = (time.perf_counter() - t0) / n
+    threads = max(1, min(oracle.max_threads(), cfg.num_kv_heads))
+
+    def timed(budget):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            step()
+            n += 1
+            if time.perf_counter() - t0 >= budget:
+                break
+        return (time.perf_counter() - t0) / n, n
+
+    default_threads = oracle.max_threads()
+    oracle.set_threads(threads)
+    dt, n = timed(budget_s)
+    oracle.set_threads(1)
+    dt1, n1 = timed(single_budget_s)
+    oracle.set_threads(default_threads)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"1 of {cfg.batch} sequences (all {cfg.num_kv_heads} kv heads, "
                       f"{int(lay.context_lens[0])} tokens): append of the step's new token + fp64 decode "
-                      f"attention; {n} repetitions in {n * dt:.1f} s"}
+                      f"attention; {n} repetitions in {n * dt:.1f} s on {threads} threads",
+            "single_thread": {"value": round(nbytes / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"the same sample on one thread, {n1} repetitions in {n1 * dt1:.1f} s"},
+            "host_cpus": os.cpu_count()}
 
 
 def run_reference(args):

@@ -81,6 +81,8 @@ def lib():
         L.orc_e4m3_encode_array.argtypes = [P, i64, P]
         L.orc_e4m3_decode_array.argtypes = [P, i64, P]
         L.orc_fp8_append.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, i32, i32]
+        L.orc_set_threads.argtypes = [i32]
+        L.orc_max_threads.restype = i32
         L.orc_fp8_decode_attention.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                                i32, i32, f64, P, i32, P]
     return _lib
@@ -260,3 +262,13 @@ def fp8_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tables, co
                                         _p(sel), 0 if sel is None else sel.size, _p(out))
     assert st == OK, f"oracle fp8_decode_attention failed ({st})"
     return out
+
+
+# ---------------------------------------------------------------- threads (timing only)
+def set_threads(n: int) -> None:
+    """Thread count of the oracle's OpenMP loops; no result depends on it."""
+    lib().orc_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().orc_max_threads())

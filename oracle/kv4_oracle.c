@@ -39,6 +39,9 @@
 #include <stdlib.h>
 #include <string.h>
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORC_OK 0
 #define ORC_BAD_ARG 1
@@ -583,4 +586,24 @@ int64_t orc_quantize_vectors(const uint16_t* x, int64_t n, int D, uint8_t* codes
     if (st != ORC_OK) inexact += 1;
   }
   return inexact;
+}
+
+/* ------------------------------------------------------------------ */
+/* Thread count of the OpenMP loops above.  Only the timing of the CPU  */
+/* baseline uses it; no result depends on the thread count.             */
+/* ------------------------------------------------------------------ */
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int orc_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }
