@@ -164,6 +164,23 @@ def test_group_exponent_puts_amax_in_top_binade():
     assert oracle.group_exponent(np.full(32, 2.0 ** 126, np.float32)) == 124
 
 
+def test_zero_vectors_quantise_to_plus_zero_codes():
+    """An all-zero vector, of either sign, rotates to an exact zero: every group
+    gets exponent -127 (scale byte 0) and every code is +0, since the exact
+    matrix product of zeros has no sign (the sign bit is kept only for nonzero
+    values that round to zero)."""
+    for z in (0.0, -0.0):
+        x = torch.full((1, 1, 128), z, dtype=torch.bfloat16)
+        codes, expo, bad = oracle.quantize_vectors(x)
+        assert bad == 0
+        assert np.all(codes == 0) and np.all(expo == -127)
+    # a nonzero negative value far below the group's scale rounds to -0 (code 0b1000)
+    y = np.zeros(32, np.float32)
+    y[0], y[1] = 4.0, -2.0 ** -10
+    codes, expo = oracle.quantize_rotated(y)
+    assert expo[0] == 0 and codes[0] == 0b0110 and codes[1] == 0b1000 and np.all(codes[2:] == 0)
+
+
 def test_on_grid_groups_round_trip_exactly():
     rng = np.random.default_rng(11)
     grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
