@@ -497,12 +497,15 @@ def oracle_sample(cfg, lay, n_seqs: int, head=None):
 
 
 def cpu_baseline(cfg, lay, budget_s: float = 12.0, single_budget_s: float = 4.0):
-    """The oracle on one sequence of the workload (all kv heads): its OpenMP loop
-    runs over the sequence's (sequence, kv head) pairs, so it uses at most that
-    many host threads; a single-thread figure is timed beside it."""
+    """The oracle on the first sequences of the workload (all kv heads): its
+    OpenMP loop runs over the sample's (sequence, kv head) pairs, so the sample
+    holds enough sequences to give every host thread one pair; a single-thread
+    figure is timed beside it."""
     import oracle
-    step, nbytes = oracle_sample(cfg, lay, 1)
-    threads = max(1, min(oracle.max_threads(), cfg.num_kv_heads))
+    host = oracle.max_threads()
+    n_seqs = max(1, min(cfg.batch, -(-host // cfg.num_kv_heads)))
+    step, nbytes = oracle_sample(cfg, lay, n_seqs)
+    threads = max(1, min(host, n_seqs * cfg.num_kv_heads))
 
     def timed(budget):
         n, t0 = 0, time.perf_counter()
@@ -520,9 +523,9 @@ def cpu_baseline(cfg, lay, budget_s: float = 12.0, single_budget_s: float = 4.0)
     dt1, n1 = timed(single_budget_s)
     oracle.set_threads(default_threads)
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"1 of {cfg.batch} sequences (all {cfg.num_kv_heads} kv heads, "
-                      f"{int(lay.context_lens[0])} tokens): append of the step's new token + fp64 decode "
-                      f"attention; {n} repetitions in {n * dt:.1f} s on {threads} threads",
+            "sample": f"{n_seqs} of {cfg.batch} sequences (all {cfg.num_kv_heads} kv heads, "
+                      f"{int(lay.context_lens[:n_seqs].sum())} tokens): append of the step's new tokens + fp64 "
+                      f"decode attention; {n} repetitions in {n * dt:.1f} s on {threads} threads",
             "single_thread": {"value": round(nbytes / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
                               "sample": f"the same sample on one thread, {n1} repetitions in {n1 * dt1:.1f} s"},
             "host_cpus": os.cpu_count()}

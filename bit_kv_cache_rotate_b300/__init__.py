@@ -26,14 +26,17 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libkv4.so")
 
 KV4_OK, KV4_ERR_INVALID_ARG, KV4_ERR_UNSUPPORTED, KV4_ERR_CUDA, KV4_ERR_DEVICE_BOUNDS = range(5)
-KV4_DEVERR_PAGE, KV4_DEVERR_CONTEXT, KV4_DEVERR_SLOT = 1, 2, 4
+KV4_DEVERR_PAGE, KV4_DEVERR_CONTEXT, KV4_DEVERR_SLOT, KV4_DEVERR_TIMEOUT = 1, 2, 4, 8
+# kernel choices and test controls of kv4_decode_attention_select (include/kv4.h)
+KV4_KERNEL_AUTO, KV4_KERNEL_WARP_MMA, KV4_KERNEL_EXTEND, KV4_KERNEL_LATENT, KV4_KERNEL_GENERAL = range(5)
+KV4_DIAG_EXPIRE_FIRST_WAIT = 1
 KV4_MAX_Q_PER_SEQ = 4096  # include/kv4.h
 PAGE_SIZE = 16
 
 EXPORTS = ("kv4_status_string", "kv4_cache_bytes", "kv4_append_quantize", "kv4_decode_auto_splits",
            "kv4_decode_workspace_bytes", "kv4_decode_attention", "kv4_decode_partials", "kv4_split_combine",
            "fp8_cache_bytes", "fp8_append_quantize", "fp8_decode_attention",
-           "kv4_decode_attention_noalloc")
+           "kv4_decode_attention_noalloc", "kv4_decode_attention_select", "kv4_decode_partials_prefix")
 
 
 class Kv4Error(RuntimeError):
@@ -67,6 +70,9 @@ def _load() -> ctypes.CDLL:
     L.kv4_decode_partials.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
                                       P, sz, P, P]
     L.kv4_decode_partials.restype = i32
+    L.kv4_decode_partials_prefix.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                             P, sz, P, P]
+    L.kv4_decode_partials_prefix.restype = i32
     L.fp8_decode_attention.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
                                        i32, P, sz, P, P, P]
     L.fp8_decode_attention.restype = i32
@@ -75,6 +81,9 @@ def _load() -> ctypes.CDLL:
     L.kv4_decode_attention_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32,
                                                i32, P, P, P]
     L.kv4_decode_attention_noalloc.restype = i32
+    L.kv4_decode_attention_select.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                              P, sz, P, P, i32, i32, P]
+    L.kv4_decode_attention_select.restype = i32
     return L
 
 
@@ -185,6 +194,33 @@ def kv4_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
     return out
 
 
+def kv4_decode_attention_select(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor | None,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int,
+                                num_pages: int, softmax_scale: float, kernel: int, diag_flags: int = 0,
+                                num_splits: int = 0, workspace_buf: torch.Tensor | None = None,
+                                out: torch.Tensor | None = None, dev_error: torch.Tensor | None = None,
+                                page_size: int = PAGE_SIZE, stream=None) -> torch.Tensor:
+    """kv4_decode_attention with an explicit split kernel (KV4_KERNEL_*) and
+    test controls (KV4_DIAG_*), for tests and measurements."""
+    _dev(q, "q", torch.bfloat16)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(context_lens, "context_lens", torch.int32)
+    B, T, Hq, D = q.shape
+    max_pages = block_tables.shape[1]
+    S = num_splits or kv4_decode_auto_splits(B, T, Hq, num_kv_heads, D, page_size, max_pages)
+    if workspace_buf is None:
+        workspace_buf = workspace(B, T, Hq, D, S, device=q.device)
+    if out is None:
+        out = torch.empty((B, T, Hq, D), dtype=torch.float32, device=q.device)
+    st = lib().kv4_decode_attention_select(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                          _ptr(context_lens), B, T, Hq, num_kv_heads, D, page_size, max_pages,
+                                          num_pages, float(softmax_scale), S, _ptr(workspace_buf),
+                                          workspace_buf.numel(), _ptr(out), _ptr(dev_error), int(kernel),
+                                          int(diag_flags), _stream(stream))
+    _check("kv4_decode_attention_select", st)
+    return out
+
+
 def kv4_decode_partials(q, k_cache, v_cache, block_tables, context_lens, num_kv_heads: int,
                         num_pages: int, softmax_scale: float, num_splits: int, workspace_buf,
                         dev_error=None, page_size: int = PAGE_SIZE, stream=None) -> None:
@@ -196,6 +232,21 @@ def kv4_decode_partials(q, k_cache, v_cache, block_tables, context_lens, num_kv_
                                    _ptr(workspace_buf), workspace_buf.numel(), _ptr(dev_error),
                                    _stream(stream))
     _check("kv4_decode_partials", st)
+
+
+def kv4_decode_partials_prefix(q, k_cache, v_cache, block_tables, context_lens, num_kv_heads: int,
+                               num_pages: int, softmax_scale: float, num_splits: int, workspace_buf,
+                               dev_error=None, page_size: int = PAGE_SIZE, stream=None) -> None:
+    """Split stage over a leading share of each sequence (every cached token
+    precedes the queries and is visible to all of them): the non-final shares
+    of a sequence split across devices (see seqsplit)."""
+    B, T, Hq, D = q.shape
+    st = lib().kv4_decode_partials_prefix(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                          _ptr(context_lens), B, T, Hq, num_kv_heads, D, page_size,
+                                          block_tables.shape[1], num_pages, float(softmax_scale), num_splits,
+                                          _ptr(workspace_buf), workspace_buf.numel(), _ptr(dev_error),
+                                          _stream(stream))
+    _check("kv4_decode_partials_prefix", st)
 
 
 def split_views(workspace_buf, B, T, Hq, D, S):

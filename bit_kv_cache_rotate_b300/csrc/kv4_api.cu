@@ -1,7 +1,6 @@
 // kv4_api.cu -- host side of libkv4: argument validation, split choice and
 // kernel dispatch behind the extern "C" entry points declared in kv4.h.
 #include <math.h>
-#include <stdlib.h>
 
 #include "kv4_common.cuh"
 
@@ -144,7 +143,8 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
                                 int D, int P, int max_pages, int num_pages, float softmax_scale,
                                 int num_splits, void* workspace, size_t workspace_bytes,
                                 float* out, int32_t* dev_error, cudaStream_t st,
-                                bool combine = true) {
+                                bool combine = true, int kernel = KV4_KERNEL_AUTO, int diag = 0,
+                                bool causal = true) {
   kv4_status s = check_decode_shape(batch, T, Hq, Hkv, D, P, max_pages, num_pages);
   if (s != KV4_OK) return s;
   if (batch == 0) return KV4_OK;
@@ -192,33 +192,49 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   const double log2e = 1.4426950408889634;
   a.qscale = (float)(softmax_scale * log2e * (fp8 ? 1.0 : inv_sqrt_dim(D)));
 
-  cudaError_t e;
-  // The warp-MMA kernel is the default tensor-core path; the tcgen05 block-
-  // scaled kernel serves the same shapes when KV4_DECODE_TCGEN05=1 (it was
-  // measured slower at batch 32, 32K context).
-  const char* tc_env = getenv("KV4_DECODE_TCGEN05");
-  const bool use_tc = tc_env != nullptr && tc_env[0] == '1';
-  // Extend steps (more query rows than the warp-MMA kernel holds per CTA) run
-  // on the tcgen05 extend kernel; KV4_EXTEND_WARPMMA=1 keeps them on the
-  // warp-MMA kernel's position tiles instead.
-  const char* xw_env = getenv("KV4_EXTEND_WARPMMA");
-  const bool extend_warp = xw_env != nullptr && xw_env[0] == '1';
+  a.diag = diag;
+  a.causal = causal ? 1 : 0;
   a.pos_split = 0;
   a.pos_tile = 1;
-  if (!fp8 && use_tc && kv4::tc_path_supported(D, G, T, latent)) {
-    e = kv4::launch_decode_tc(a, st);
-  } else if (!fp8 && !extend_warp && kv4::extend_tc_supported(D, G, T, latent)) {
-    e = kv4::launch_extend_tc(a, st);
-  } else if (!fp8 && kv4::mla_path_supported(D, G, T, latent)) {
-    e = kv4::launch_decode_mla(a, st);
-  } else if (!fp8 && kv4::fast_path_supported(D, G, T, latent)) {
-    e = kv4::launch_decode_fast(D, a, st);  // chooses row blocks or pos_split
-  } else if (fp8 && kv4::fp8_fast_path_supported(D, G, T)) {
-    a.pos_split = T * G > 8 ? 1 : 0;
-    e = kv4::launch_decode_fp8_fast(a, st);
-  } else {
-    if (T * G > kv4::ref_max_rows(D)) return KV4_ERR_UNSUPPORTED;
-    e = kv4::launch_decode_ref(fp8, D, a, st);
+
+  // Kernel choice.  By shape: extend steps (more query rows than the warp-MMA
+  // kernel holds per CTA) on the tcgen05 extend kernel, the latent cache on the
+  // latent kernel, head_dim 128 with up to 8 query heads per kv head on the
+  // warp-MMA kernel, everything else on the general kernel.  An explicit
+  // choice (kv4_decode_attention_select) must serve the shape.
+  const bool ok_ext = !fp8 && kv4::extend_tc_supported(D, G, T, latent);
+  const bool ok_mla = !fp8 && kv4::mla_path_supported(D, G, T, latent);
+  const bool ok_warp = fp8 ? kv4::fp8_fast_path_supported(D, G, T) : kv4::fast_path_supported(D, G, T, latent);
+  const bool ok_gen = T * G <= kv4::ref_max_rows(D);
+  int k = kernel;
+  if (k == KV4_KERNEL_AUTO)
+    k = ok_ext ? KV4_KERNEL_EXTEND : ok_mla ? KV4_KERNEL_LATENT : ok_warp ? KV4_KERNEL_WARP_MMA
+                                                                           : KV4_KERNEL_GENERAL;
+  cudaError_t e;
+  switch (k) {
+    case KV4_KERNEL_EXTEND:
+      if (!ok_ext) return KV4_ERR_UNSUPPORTED;
+      e = kv4::launch_extend_tc(a, st);
+      break;
+    case KV4_KERNEL_LATENT:
+      if (!ok_mla) return KV4_ERR_UNSUPPORTED;
+      e = kv4::launch_decode_mla(a, st);
+      break;
+    case KV4_KERNEL_WARP_MMA:
+      if (!ok_warp) return KV4_ERR_UNSUPPORTED;
+      if (fp8) {
+        a.pos_split = T * G > 8 ? 1 : 0;
+        e = kv4::launch_decode_fp8_fast(a, st);
+      } else {
+        e = kv4::launch_decode_fast(D, a, st);  // chooses row blocks or pos_split
+      }
+      break;
+    case KV4_KERNEL_GENERAL:
+      if (!ok_gen) return KV4_ERR_UNSUPPORTED;
+      e = kv4::launch_decode_ref(fp8, D, a, st);
+      break;
+    default:
+      return KV4_ERR_INVALID_ARG;
   }
   if (e != cudaSuccess) return KV4_ERR_CUDA;
   if (!combine) return KV4_OK;
@@ -240,6 +256,20 @@ kv4_status kv4_decode_attention(const void* q, const uint8_t* k_cache, const uin
                        workspace_bytes, out, dev_error, (cudaStream_t)stream);
 }
 
+kv4_status kv4_decode_attention_select(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens,
+                                       int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int page_size, int max_pages_per_seq,
+                                       int num_pages, float softmax_scale, int num_splits,
+                                       void* workspace, size_t workspace_bytes, float* out,
+                                       int32_t* dev_error, int kernel, int diag_flags,
+                                       kv4_stream_t stream) {
+  return decode_common(false, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens,
+                       batch, q_per_seq, num_q_heads, num_kv_heads, head_dim, page_size,
+                       max_pages_per_seq, num_pages, softmax_scale, num_splits, workspace,
+                       workspace_bytes, out, dev_error, (cudaStream_t)stream, true, kernel, diag_flags);
+}
+
 kv4_status kv4_decode_partials(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
                                const int32_t* block_tables, const int32_t* context_lens,
                                int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
@@ -250,6 +280,20 @@ kv4_status kv4_decode_partials(const void* q, const uint8_t* k_cache, const uint
                        batch, q_per_seq, num_q_heads, num_kv_heads, head_dim, page_size,
                        max_pages_per_seq, num_pages, softmax_scale, num_splits, workspace,
                        workspace_bytes, nullptr, dev_error, (cudaStream_t)stream, false);
+}
+
+kv4_status kv4_decode_partials_prefix(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int page_size, int max_pages_per_seq,
+                                      int num_pages, float softmax_scale, int num_splits,
+                                      void* workspace, size_t workspace_bytes, int32_t* dev_error,
+                                      kv4_stream_t stream) {
+  return decode_common(false, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens,
+                       batch, q_per_seq, num_q_heads, num_kv_heads, head_dim, page_size,
+                       max_pages_per_seq, num_pages, softmax_scale, num_splits, workspace,
+                       workspace_bytes, nullptr, dev_error, (cudaStream_t)stream, false,
+                       KV4_KERNEL_AUTO, 0, false);
 }
 
 kv4_status fp8_decode_attention(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,

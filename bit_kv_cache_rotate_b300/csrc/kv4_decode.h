@@ -23,6 +23,11 @@ struct DecodeArgs {
   int pos_split;           // 1: query positions split over CTAs, pos_tile per CTA
   int pos_tile;            //    (grid x = S * ceil(T / pos_tile), split-major)
   float qscale;            // softmax_scale * log2(e), times 1/sqrt(D) for the 4-bit rotation
+  int diag;                // KV4_DIAG_* test controls (0 in normal calls)
+  int causal;              // 1: the last T cached tokens are the query positions (causal among
+                           //    them); 0: every cached token precedes the queries and is
+                           //    visible to all of them (a leading share of a sequence split
+                           //    across devices); context lengths may then be 0
 };
 
 // Splits per sequence: about seven CTAs per SM in all (1.75 waves of the
@@ -49,8 +54,6 @@ bool fast_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st);
 bool mla_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st);
-bool tc_path_supported(int D, int G, int T, bool latent);
-cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 bool fp8_fast_path_supported(int D, int G, int T);
 cudaError_t launch_decode_fp8_fast(const DecodeArgs& a, cudaStream_t st);
 bool extend_tc_supported(int D, int G, int T, bool latent);

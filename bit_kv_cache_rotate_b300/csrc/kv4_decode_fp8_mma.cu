@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
   const int G = a.Hq / a.Hkv;
   const int R = Tc * G;
   const int L_seq = a.context_lens[b];
-  const int L = L_seq - (a.T - Tc) + j0;  // tokens visible to this CTA's last position
+  const int L = a.causal ? L_seq - (a.T - Tc) + j0 : L_seq;  // tokens visible to this CTA's last position
   const size_t row0 = ((size_t)b * a.T + j0) * a.Hq;
   uint8_t* stage = smem_raw + w * kStageBytes;
   uint16_t* qt = reinterpret_cast<uint16_t*>(smem_raw + kWarps * kStageBytes);
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
       if (lane == 0) a.part_lse[rr] = -INFINITY;
     }
   };
-  if (L_seq < a.T || L_seq > a.max_pages * kPage) {
+  if (L_seq < (a.causal ? a.T : 0) || L_seq > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
     return;
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_fp8_mma_kernel(DecodeArgs 
     if (lane == 0) {
       // score*log2e = (q*2^sigma . k_e4m3) * 2^-sigma * k_scale * softmax_scale*log2e
       row_c[r] = a.qscale * a.k_scale[h] * __uint_as_float((uint32_t)(127 - sigma) << 23);
-      row_limit[r] = r < R ? L - Tc + 1 + r / G : 0x7fffffff;
+      row_limit[r] = r < R ? (a.causal ? L - Tc + 1 + r / G : L) : 0x7fffffff;
     }
   }
   __syncthreads();

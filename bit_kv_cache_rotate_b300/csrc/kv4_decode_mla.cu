@@ -55,6 +55,53 @@ __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
   return y;
 }
 
+// P.V of one chunk whose V scales span more binades than the f16 factors hold
+// (a V scale more than 14 binades below the group reference): the scale is
+// folded into P in fp32, x = p * 2^(e - E_G) with E_G the chunk's largest
+// exponent of the group, and x and the codes go through bf16 MMAs, which keep
+// fp32's exponent range.  Same fragment layout as the f16 path; p[nn][k] holds
+// tokens 8nn + 2t + (k & 1) of rows g (k < 2) and g + 8.
+__device__ __forceinline__ void pv_bf16(float (&o)[8][2][4], const float (&p)[4][4], const uint8_t* stage,
+                                        uint32_t eref, int w, int g, int t) {
+#pragma unroll
+  for (int G4 = 0; G4 < 4; ++G4) {
+    const int E = (int)((eref >> (8 * G4)) & 0xFFu);
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      // B fragments: [rows 0-7 | 8-15][b0: tokens 16kk + 2t (+1), b1: 16kk + 8 + 2t (+1)]
+      uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+      for (int bb = 0; bb < 2; ++bb) {
+        const int tok = 16 * kk + 8 * bb + 2 * t;
+        const uint8_t* sp = stage + (tok >> 4) * kBlk + kCodeBytes + (tok & 15) * 16 + 4 * w + G4;
+        const float f0 = pow2_diff(sp[0], E), f1 = pow2_diff(sp[16], E);
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+          split_bf16x2(p[2 * kk + bb][2 * hr] * f0, p[2 * kk + bb][2 * hr + 1] * f1, bh[hr][bb], bl[hr][bb]);
+      }
+      uint32_t wv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int nn = 2 * kk + u;
+        wv[u] = *reinterpret_cast<const uint32_t*>(stage + (nn >> 1) * kBlk + (((nn & 1) * 16 + 4 * w + G4) * 128) +
+                                                   g * 16 + 4 * t);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t a0 = movtrans(f16x2_to_bf16x2(e2m1x2_to_f16x2(wv[0], 2 * j)));
+        const uint32_t a1 = movtrans(f16x2_to_bf16x2(e2m1x2_to_f16x2(wv[0], 2 * j + 1)));
+        const uint32_t a2 = movtrans(f16x2_to_bf16x2(e2m1x2_to_f16x2(wv[1], 2 * j)));
+        const uint32_t a3 = movtrans(f16x2_to_bf16x2(e2m1x2_to_f16x2(wv[1], 2 * j + 1)));
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          mma_bf16(o[2 * G4 + j][hr], a0, a1, a2, a3, bh[hr][0], bh[hr][1]);
+          mma_bf16(o[2 * G4 + j][hr], a0, a1, a2, a3, bl[hr][0], bl[hr][1]);
+        }
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float row_c[kRows];
@@ -75,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
       if (lane == 0) a.part_lse[rr] = -INFINITY;
     }
   };
-  if (L < a.T || L > a.max_pages * kPage) {
+  if (L < (a.causal ? a.T : 0) || L > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
     return;
@@ -166,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
     if (lane == 0) {
       // score*log2e = (q*2^sigma . code * 2^e) * 2^-sigma * softmax_scale*log2e/sqrt(D)
       row_c[r] = a.qscale * __uint_as_float((uint32_t)(127 - sigma) << 23);
-      row_limit[r] = r < R ? L - a.T + 1 + r / G : 0x7fffffff;
+      row_limit[r] = r < R ? (a.causal ? L - a.T + 1 + r / G : L) : 0x7fffffff;
     }
   }
   __syncthreads();
@@ -184,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
     for (int n = 0; n < 2; ++n) o[m][n][0] = o[m][n][1] = o[m][n][2] = o[m][n][3] = 0.0f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
   uint32_t eref = 0;
+  const int first_limit = (a.diag & KV4_DIAG_EXPIRE_FIRST_WAIT) ? 0 : kSpinLimit;
   bool timed_out = false;
   int waited = 0;
   float* ktab = reinterpret_cast<float*>(smem + kOffKTab + w * 512);        // [4 groups][32 tokens]
@@ -192,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
 #pragma unroll 1
   for (int c = 0; c < n_chunks; ++c) {
     const int st = c % kStages;
-    if (!mbar_wait(&full[st], (uint32_t)((c / kStages) & 1))) timed_out = true;
+    if (!mbar_wait(&full[st], (uint32_t)((c / kStages) & 1), c == 0 ? first_limit : kSpinLimit)) timed_out = true;
     if (__syncthreads_or(timed_out)) {
       timed_out = true;
       break;
@@ -204,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
     const bool edge = nv < kChunkPages || (pg + kChunkPages) * kPage > min_limit;
 
     // ---- scale tables of this warp's 4 groups: lane = token (page lane>>4)
-    uint32_t eold;
+    uint32_t eold, enew = 0;
+    bool slow;
     {
       const int pi = lane >> 4, tk = lane & 15;
       const bool ok = pi < nv && (pg + pi) * kPage + tk < L;
@@ -223,9 +272,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
         eref = __vmaxu4(eref, cm);
         lim = __vaddus4(eref, 0x07070707u);
       }
-      const uint32_t av = __vsubus4(0x16161616u, __vsubus4(lim, word));  // f16 exponent fields
+      // f16 exponent fields (tokens past the context take lim's in-window field)
+      const uint32_t av = __vsubus4(0x16161616u, __vsubus4(lim, ok ? word : lim));
       const uint32_t an = __shfl_down_sync(0xffffffffu, av, 1);          // token 2p+1
-      if ((lane & 1) == 0) {
+      // A zero field: a V scale more than 14 binades below the reference (or
+      // an all-zero group).  Such a chunk takes the bf16 path with the
+      // reference re-taken from the chunk (as in the 4-bit decode kernel).
+      slow = __any_sync(0xffffffffu, has_zero_byte(av) != 0u);
+      if (slow) {
+        uint32_t cm = word;
+#pragma unroll
+        for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
+        const uint32_t none = __vcmpeq4(cm, 0u);
+        enew = (__vmaxu4(cm, __vsubus4(eold, 0x5A5A5A5Au)) & ~none) | (eold & none);
+      } else if ((lane & 1) == 0) {
         uint4 vp;
         vp.x = __byte_perm(__byte_perm(av, an, 0x0040), 0, 0x5140) << 10;
         vp.y = __byte_perm(__byte_perm(av, an, 0x0051), 0, 0x5140) << 10;
@@ -346,12 +406,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
     // held by lanes 8t and 8t + 4
     const float a00 = __shfl_sync(0xffffffffu, alpha[0], 8 * t), a01 = __shfl_sync(0xffffffffu, alpha[0], 8 * t + 4);
     const float a10 = __shfl_sync(0xffffffffu, alpha[1], 8 * t), a11 = __shfl_sync(0xffffffffu, alpha[1], 8 * t + 4);
-    if (__any_sync(0xffffffffu, a00 != 1.0f || a01 != 1.0f || a10 != 1.0f || a11 != 1.0f || eold != eref)) {
+    if (slow || __any_sync(0xffffffffu, a00 != 1.0f || a01 != 1.0f || a10 != 1.0f || a11 != 1.0f || eold != eref)) {
       const uint32_t dl = __vsubus4(eref, eold);
 #pragma unroll
       for (int G4 = 0; G4 < 4; ++G4) {
         const int ex = 127 - (int)((dl >> (8 * G4)) & 0xFFu);
-        const float f = ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f;
+        // slow chunks: the reference moves to enew, up or down
+        const float f = slow ? pow2_diff((eold >> (8 * G4)) & 0xFFu, (int)((enew >> (8 * G4)) & 0xFFu))
+                             : (ex > 0 ? __uint_as_float((uint32_t)ex << 23) : 0.0f);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           float (&o0)[4] = o[2 * G4 + j][0];
@@ -367,6 +429,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
         }
       }
     }
+    if (slow) eref = enew;
+    if (slow) {
+      pv_bf16(o, p, stage, eref, w, g, t);
+    } else {
     // ---- P fragments: k-step kk = tokens 16kk..16kk+15 = n-tiles 2kk, 2kk+1;
     // b0 = tokens 16kk + 2t (+1), b1 = 16kk + 8 + 2t (+1); [kk][rows 0-7 | 8-15][b0, b1]
     uint32_t ph[2][2][2], pl[2][2][2];
@@ -427,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mla_kernel(DecodeArgs a) {
         }
       }
     }
+    }  // fast path
   }
 
   if (timed_out) {

@@ -91,6 +91,59 @@ struct Smem {
   }
 };
 
+// P.V of one chunk for chunks whose V scales span more binades than the f16
+// factors hold (a V scale more than 14 binades below the group reference).
+// The scale is folded into P in fp32, x = p * 2^(e_v - E_G) with E_G the
+// group's reference (the chunk's largest V exponent), and x and the V codes
+// go through bf16 MMAs: bf16 keeps fp32's exponent range, so every token's
+// value survives down to 2^-126 of the reference; x carries about 16
+// significant bits as bf16 hi + lo.  vbase: the staged V block of page t
+// (thread quad index); same fragment layout as the f16 path.
+template <int RB>
+__device__ __forceinline__ void pv_bf16(float (&o)[RB][8][4], const float2 (&p)[RB][8], const uint8_t* vbase,
+                                        uint32_t eref, int g) {
+  uint32_t sw[16];  // the V scale words of the page's 16 tokens, 4 groups each
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 x = *reinterpret_cast<const uint4*>(vbase + kCodeBytes + 16 * i);
+    sw[4 * i] = x.x;
+    sw[4 * i + 1] = x.y;
+    sw[4 * i + 2] = x.z;
+    sw[4 * i + 3] = x.w;
+  }
+#pragma unroll
+  for (int G4 = 0; G4 < 4; ++G4) {
+    const int E = (int)((eref >> (8 * G4)) & 0xFFu);
+    const uint2 rA0 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + g) * (kPage / 2));
+    const uint2 rB0 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + g + 8) * (kPage / 2));
+    const uint2 rA1 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + 16 + g) * (kPage / 2));
+    const uint2 rB1 = *reinterpret_cast<const uint2*>(vbase + (32 * G4 + 16 + g + 8) * (kPage / 2));
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const int b0 = (2 * c4) & 3, b1 = (2 * c4 + 1) & 3;
+      const uint32_t wA0 = c4 < 2 ? rA0.x : rA0.y, wB0 = c4 < 2 ? rB0.x : rB0.y;
+      const uint32_t wA1 = c4 < 2 ? rA1.x : rA1.y, wB1 = c4 < 2 ? rB1.x : rB1.y;
+      const uint32_t x00 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wA0, b0)), x01 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wB0, b0));
+      const uint32_t x02 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wA0, b1)), x03 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wB0, b1));
+      const uint32_t x10 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wA1, b0)), x11 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wB1, b0));
+      const uint32_t x12 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wA1, b1)), x13 = f16x2_to_bf16x2(e2m1x2_to_f16x2(wB1, b1));
+      float f[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f[i] = pow2_diff((sw[4 * c4 + i] >> (8 * G4)) & 0xFFu, E);
+#pragma unroll
+      for (int rb = 0; rb < RB; ++rb) {
+        uint32_t h01, l01, h23, l23;
+        split_bf16x2(p[rb][2 * c4].x * f[0], p[rb][2 * c4].y * f[1], h01, l01);
+        split_bf16x2(p[rb][2 * c4 + 1].x * f[2], p[rb][2 * c4 + 1].y * f[3], h23, l23);
+        mma_bf16(o[rb][2 * G4], x00, x01, x02, x03, h01, h23);
+        mma_bf16(o[rb][2 * G4 + 1], x10, x11, x12, x13, h01, h23);
+        mma_bf16(o[rb][2 * G4], x00, x01, x02, x03, l01, l23);
+        mma_bf16(o[rb][2 * G4 + 1], x10, x11, x12, x13, l01, l23);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 // Rows: the R = T*G query rows of one kv head, R <= 8 * RB (row r -> position
 // r / G, query head h*G + r % G), in RB blocks of 8 MMA rows; unused rows
@@ -120,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
   const int G = a.Hq / a.Hkv;
   const int R = Tc * G;
   const int L_seq = a.context_lens[b];
-  const int L = L_seq - (a.T - Tc) + j0;  // tokens visible to this CTA's last position
+  const int L = a.causal ? L_seq - (a.T - Tc) + j0 : L_seq;  // tokens visible to this CTA's last position
   const size_t row0 = ((size_t)b * a.T + j0) * a.Hq;
 
   auto row_index = [&](int r) -> size_t {  // flat (b, j, hq) row of query row r
@@ -133,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
       if (lane == 0) a.part_lse[rr] = -INFINITY;
     }
   };
-  if (L_seq < a.T || L_seq > a.max_pages * kPage) {
+  if (L_seq < (a.causal ? a.T : 0) || L_seq > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
     return;
@@ -245,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     if (lane == 0) {
       // score*log2e = (q*2^sigma . code * 2^e) * 2^-sigma * softmax_scale*log2e/sqrt(D)
       row_c[r] = a.qscale * __uint_as_float((uint32_t)(127 - sigma) << 23);
-      row_limit[r] = r < R ? L - Tc + 1 + r / G : 0x7fffffff;
+      row_limit[r] = r < R ? (a.causal ? L - Tc + 1 + r / G : L) : 0x7fffffff;
     }
   }
   __syncthreads();
@@ -295,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
 
   float* ktab = sm.ktab(w);
   uint32_t* vtab = sm.vtab(w);
+  const int first_limit = (a.diag & KV4_DIAG_EXPIRE_FIRST_WAIT) ? 0 : kSpinLimit;
   bool timed_out = false;
   int it_fail = 0;
 
@@ -304,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     // page ids for the refill of this stage, loaded now to hide their latency
     const int cn = c + kWarps * kStages;
     const int next_page = cn < n_chunks ? chunk_page(cn) : 0;
-    if (!mbar_wait(&bars[w * kStages + st], parity)) {
+    if (!mbar_wait(&bars[w * kStages + st], parity, it == 0 ? first_limit : kSpinLimit)) {
       timed_out = true;
       it_fail = it;
       break;
@@ -315,18 +369,20 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     const bool edge = nv < kPagesPerChunk || (pg + kPagesPerChunk) * kPage > min_limit;
 
     // ---- scale tables: lane -> page lane>>3, token pair lane&7
-    uint32_t eold;
+    uint32_t eold, enew = 0;
+    bool slow;
     {
       const int pp = lane >> 3, pr = lane & 7, tk = 2 * pr;
       const int pos = (pg + pp) * kPage + tk;
       uint32_t k0 = 0, k1 = 0, v0 = 0, v1 = 0;
+      const bool ok0 = pp < nv && pos < L, ok1 = pp < nv && pos + 1 < L;
       if (pp < nv) {
         const uint8_t* kb = stg + pp * kBlkStride + kCodeBytes;
         const uint8_t* vb = stg + kPagesPerChunk * kBlkStride + pp * kVStride + kCodeBytes;
         const uint2 kk = *reinterpret_cast<const uint2*>(kb + tk * 4);
         const uint2 vv = *reinterpret_cast<const uint2*>(vb + tk * 4);
-        if (pos < L) { k0 = kk.x; v0 = vv.x; }
-        if (pos + 1 < L) { k1 = kk.y; v1 = vv.y; }
+        if (ok0) { k0 = kk.x; v0 = vv.x; }
+        if (ok1) { k1 = kk.y; v1 = vv.y; }
       }
       // V reference exponent per group (Eref): fixed from the warp's first
       // chunk, so the usual chunk needs no reduction.  The f16 scale factors
@@ -359,21 +415,35 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
       kt[1] = f23;
       // V scale pairs 2^(e_v - Eref_G) as f16x2 (token tk low half, tk+1 high half):
       // f16 exponent field 15 + e_v - Eref per byte, in [0, 22] here (as
-      // 22 - (Eref + 7 - e_v), both differences non-negative); values
-      // below 2^-14 of the reference flush to zero.  A zero scale byte belongs
-      // to an all-zero-code group, whose values are zero whatever the scale.
-      const uint32_t a0 = __vsubus4(0x16161616u, __vsubus4(lim, v0));
-      const uint32_t a1 = __vsubus4(0x16161616u, __vsubus4(lim, v1));
-      uint4 vp;
-      vp.x = __byte_perm(__byte_perm(a0, a1, 0x0040), 0, 0x5140) << 10;
-      vp.y = __byte_perm(__byte_perm(a0, a1, 0x0051), 0, 0x5140) << 10;
-      vp.z = __byte_perm(__byte_perm(a0, a1, 0x0062), 0, 0x5140) << 10;
-      vp.w = __byte_perm(__byte_perm(a0, a1, 0x0073), 0, 0x5140) << 10;
-      uint32_t* vt = vtab + pp * (kVTabPage / 4) + pr;
-      vt[0] = vp.x;
-      vt[8] = vp.y;
-      vt[16] = vp.z;
-      vt[24] = vp.w;
+      // 22 - (Eref + 7 - e_v), both differences non-negative).  Tokens past
+      // the context take the in-window field of `lim` (their p is 0).
+      const uint32_t a0 = __vsubus4(0x16161616u, __vsubus4(lim, ok0 ? v0 : lim));
+      const uint32_t a1 = __vsubus4(0x16161616u, __vsubus4(lim, ok1 ? v1 : lim));
+      // A zero field is a V scale more than 14 binades below the reference
+      // (or a zero byte: an all-zero group); f16 cannot carry that factor, so
+      // the chunk takes the bf16 path below with a reference re-taken from the
+      // chunk itself: each group's largest V exponent of the chunk (at most 90
+      // binades below the old one, so the rescaled O stays finite).  Groups
+      // with no visible token keep their reference.
+      slow = __any_sync(0xffffffffu, (has_zero_byte(a0) | has_zero_byte(a1)) != 0u);
+      if (slow) {
+        uint32_t cm = __vmaxu4(v0, v1);
+#pragma unroll
+        for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
+        const uint32_t none = __vcmpeq4(cm, 0u);
+        enew = (__vmaxu4(cm, __vsubus4(eold, 0x5A5A5A5Au)) & ~none) | (eold & none);
+      } else {
+        uint4 vp;
+        vp.x = __byte_perm(__byte_perm(a0, a1, 0x0040), 0, 0x5140) << 10;
+        vp.y = __byte_perm(__byte_perm(a0, a1, 0x0051), 0, 0x5140) << 10;
+        vp.z = __byte_perm(__byte_perm(a0, a1, 0x0062), 0, 0x5140) << 10;
+        vp.w = __byte_perm(__byte_perm(a0, a1, 0x0073), 0, 0x5140) << 10;
+        uint32_t* vt = vtab + pp * (kVTabPage / 4) + pr;
+        vt[0] = vp.x;
+        vt[8] = vp.y;
+        vt[16] = vp.z;
+        vt[24] = vp.w;
+      }
       __syncwarp();
     }
 
@@ -485,7 +555,25 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
         a1[rb] = __shfl_sync(0xffffffffu, alpha[rb], 8 * t + 4);
         any_a |= a0[rb] != 1.0f || a1[rb] != 1.0f;
       }
-      if (__any_sync(0xffffffffu, eold != eref || any_a)) {
+      if (slow) {
+        // the reference moves to enew, up or down: factor 2^(Eold - Enew)
+#pragma unroll
+        for (int G4 = 0; G4 < 4; ++G4) {
+          const float f = pow2_diff((eold >> (8 * G4)) & 0xFFu, (int)((enew >> (8 * G4)) & 0xFFu));
+#pragma unroll
+          for (int rb = 0; rb < RB; ++rb) {
+            const float f0 = f * a0[rb], f1 = f * a1[rb];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              o[rb][2 * G4 + jj][0] *= f0;
+              o[rb][2 * G4 + jj][1] *= f1;
+              o[rb][2 * G4 + jj][2] *= f0;
+              o[rb][2 * G4 + jj][3] *= f1;
+            }
+          }
+        }
+        eref = enew;
+      } else if (__any_sync(0xffffffffu, eold != eref || any_a)) {
         const uint32_t dl = __vsubus4(eref, eold);  // Enew - Eold per group
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
@@ -511,6 +599,10 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     // The lo part matters only for large p: its MMAs run for a k-step only when
     // some p of the step (any row, any page) exceeds 2^-8; below that the f16
     // rounding of p alone stays under 2^-20 per token.
+    const uint8_t* vbase = stg + kPagesPerChunk * kBlkStride + t * kVStride;
+    if (slow) {
+      pv_bf16<RB>(o, p, vbase, enew, g);
+    } else {
     uint32_t ph[RB][4][2], pl[RB][4][2];
     bool need_lo[4];
 #pragma unroll
@@ -534,7 +626,6 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     // ---- P.V: m-tile j = dims 16j..16j+15 (group j/2); rows g, g+8 -> dims 16j+g, 16j+g+8.
     // V codes widen exactly to f16; the V scale 2^(e_v - Eref_G) multiplies the
     // P fragments of group G instead (two tokens per f16x2, as in the A fragment).
-    const uint8_t* vbase = stg + kPagesPerChunk * kBlkStride + t * kVStride;
     const uint32_t* vrow = vtab + t * (kVTabPage / 4);
 #pragma unroll
     for (int G4 = 0; G4 < 4; ++G4) {
@@ -567,6 +658,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
         }
       }
     }
+    }  // fast path
     __syncwarp();
     // refill this stage with the warp's chunk kStages ahead
     if (cn < n_chunks) {
@@ -676,19 +768,37 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st) {
   });
   if (!encode) return cudaErrorNotSupported;
   // Each cache as a 2-D tensor of rows, one (page, head) block per row: 136
-  // eight-byte elements, row stride 1088 bytes.
-  CUtensorMap kmap, vmap;
-  const cuuint64_t dims[2] = {(cuuint64_t)fast::kBlk / 8, (cuuint64_t)a_in.num_pages * a_in.Hkv};
-  const cuuint64_t strides[1] = {(cuuint64_t)fast::kBlk};
-  const cuuint32_t box[2] = {(cuuint32_t)fast::kBlk / 8, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  for (int i = 0; i < 2; ++i) {
-    if (encode(i ? &vmap : &kmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
-               const_cast<uint8_t*>(i ? a_in.v_cache : a_in.k_cache), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+  // eight-byte elements, row stride 1088 bytes.  A map holds only the address
+  // and the sizes, so the maps of the caches a host thread used last are kept
+  // and re-encoded only when the cache or its size changes (a serving loop
+  // decodes the same caches step after step).
+  struct MapCache {
+    const void* k = nullptr;
+    const void* v = nullptr;
+    cuuint64_t rows = 0;
+    CUtensorMap kmap, vmap;
+  };
+  thread_local MapCache mc;
+  const cuuint64_t rows = (cuuint64_t)a_in.num_pages * a_in.Hkv;
+  if (mc.k != a_in.k_cache || mc.v != a_in.v_cache || mc.rows != rows) {
+    mc.k = nullptr;
+    const cuuint64_t dims[2] = {(cuuint64_t)fast::kBlk / 8, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)fast::kBlk};
+    const cuuint32_t box[2] = {(cuuint32_t)fast::kBlk / 8, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    for (int i = 0; i < 2; ++i) {
+      if (encode(i ? &mc.vmap : &mc.kmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2,
+                 const_cast<uint8_t*>(i ? a_in.v_cache : a_in.k_cache), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    mc.k = a_in.k_cache;
+    mc.v = a_in.v_cache;
+    mc.rows = rows;
   }
+  const CUtensorMap& kmap = mc.kmap;
+  const CUtensorMap& vmap = mc.vmap;
   DecodeArgs a = a_in;
   const int G = a.Hq / a.Hkv;
   int R = a.T * G;

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(kRefThreads) decode_ref_kernel(DecodeArgs a) {
       if (lane == 0) a.part_lse[rr] = -INFINITY;
     }
   };
-  if (L < a.T || L > a.max_pages * kPage) {
+  if (L < (a.causal ? a.T : 0) || L > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
     return;
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kRefThreads) decode_ref_kernel(DecodeArgs a) {
       if (r < R) {
         const int j = r / G;
         const int pos = p * kPage + t;
-        const int limit = L - a.T + 1 + j;
+        const int limit = a.causal ? L - a.T + 1 + j : L;
         if (pos < limit && !bad) {
           float acc_s = 0.0f;
           const float* qr = qs + r * D;

@@ -86,7 +86,7 @@ constexpr int kPF = kRows * kChunk * 2;               // P' f16, 128 rows x 128 
 constexpr int kOffP = kOffVF + kVF;                   // [hi, lo]
 constexpr int kOffFac = kOffP + 2 * kPF;              // f16 [4 groups][128 tokens] V factors
 constexpr int kOffSfa = kOffFac + 4 * kChunk * 2;     // [kTerms][128 rows][4 groups] q scale bytes
-constexpr int kOffMisc = kOffSfa + kTerms * kRows * 4;  // [4] per-warp maxima
+constexpr int kOffMisc = kOffSfa + kTerms * kRows * 4;  // [4] per-warp maxima, [4] minima
 constexpr int kOffBar = kOffMisc + 64;                // full[kRaw], sdone[2], pvdone, drain
 constexpr int kNumBars = kRaw + 4;
 constexpr int kSmem = kOffBar + 8 * kNumBars;
@@ -131,11 +131,22 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uin
       "l"(a), "l"(b), "r"(kIdescQK), "r"(sfa), "r"(sfb), "r"(accumulate));
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+// The same P.V on bf16 operands (A and B formats 1): chunks whose V exponents
+// span more binades than f16 holds.
+constexpr uint32_t kIdescPVbf16 = kIdescPV | (1u << 7) | (1u << 10);
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate,
+                                        uint32_t idesc = kIdescPV) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(kIdescPV), "r"(accumulate));
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 __device__ __forceinline__ void commit(uint64_t* bar) {
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L_seq = a.context_lens[b];
   // tokens visible to the tile's last position; row r (position j0 + r / G)
   // sees the first L - Tc + 1 + r / G of them
-  const int L = L_seq - (a.T - Tc) + j0;
+  const int L = a.causal ? L_seq - (a.T - Tc) + j0 : L_seq;
   const size_t row0 = ((size_t)b * a.T + j0) * a.Hq;
   auto row_index = [&](int r) -> size_t { return row0 + (size_t)(r / G) * a.Hq + h * G + (r % G); };
   auto write_empty = [&]() {
@@ -221,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) a.part_lse[rr] = -INFINITY;
     }
   };
-  if (L_seq < a.T || L_seq > a.max_pages * kPage) {
+  if (L_seq < (a.causal ? a.T : 0) || L_seq > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
     return;
@@ -243,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pvdone = bars + kRaw + 2; // P.V of a chunk complete
   uint64_t* drain = bars + kRaw + 3;  // every MMA issued so far complete (after a timeout)
   int* wmax = reinterpret_cast<int*>(smem + kOffMisc);
+  int* wmin = wmax + 4;
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
@@ -374,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // this thread's row and column half
   const int my_r = 32 * qd + lane;
-  const int my_limit = my_r < R ? L - Tc + 1 + my_r / G : 0;
+  const int my_limit = my_r < R ? (a.causal ? L - Tc + 1 + my_r / G : L) : 0;
   float m_run = -INFINITY;
   float l_half = 0.0f;  // this half's share of the row sum
   float om[64];         // running O of this row's half, summed segments
@@ -387,11 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Wait for chunk c's pages; the warps of half 0 write its K scales into
   // tensor memory (token 32i + lane at column c0 + i of every quadrant).
+  const int first_limit = (a.diag & KV4_DIAG_EXPIRE_FIRST_WAIT) ? 0 : kSpinLimit;
   auto stage_k = [&](int c) {
     const int rb = c % kRaw;
     const int pg = p0 + c * kChunkPages;
     const int nv = min(kChunkPages, p1 - pg);
-    if (!mbar_wait(&full[rb], (uint32_t)((c / kRaw) & 1))) timed_out = true;
+    if (!mbar_wait(&full[rb], (uint32_t)((c / kRaw) & 1), c == 0 ? first_limit : kSpinLimit)) timed_out = true;
     if (hf == 0 && __all_sync(0xffffffffu, !timed_out)) {
       uint32_t v0[4], v1[4];
 #pragma unroll
@@ -429,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before_sync();
   if (__syncthreads_or(timed_out)) timed_out = true;
   fence_after_sync();
-  waited_full = 1;
+  // after a timeout the drain waits for chunk 0's copies again (a wait on a
+  // completed phase returns at once)
+  waited_full = timed_out ? 0 : 1;
   if (!timed_out && tid == kMmaThread) issue_qk(0);
 
 #pragma unroll 1
@@ -450,7 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t m4 = __vmaxu4(vsw, vsw >> 16);
       m4 = max(m4 & 0xFFu, (m4 >> 8) & 0xFFu);
       m4 = __reduce_max_sync(0xffffffffu, m4);
-      if (lane == 0) wmax[w] = (int)m4;
+      // smallest nonzero exponent (zero bytes: invisible tokens, all-zero groups)
+      const uint32_t nz = vsw | __vcmpeq4(vsw, 0u);
+      uint32_t n4 = __vminu4(nz, nz >> 16);
+      n4 = min(n4 & 0xFFu, (n4 >> 8) & 0xFFu);
+      n4 = __reduce_min_sync(0xffffffffu, n4);
+      if (lane == 0) {
+        wmax[w] = (int)m4;
+        wmin[w] = (int)n4;
+      }
     }
     fence_before_sync();
     if (__syncthreads_or(timed_out)) {
@@ -461,26 +484,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     waited_full = min(n_chunks, c + 2);
     if (tid == kMmaThread && c + 1 < n_chunks) issue_qk(c + 1);
     const int e_c = max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3]));
-    // V reference: set by the first chunk, raised when a chunk exceeds it by > 4
+    const int e_lo = min(min(wmin[0], wmin[1]), min(wmin[2], wmin[3]));
+    // V reference: set by the first chunk, moved to the chunk's largest
+    // exponent when that differs from it by more than 4 either way (at most 90
+    // binades down at once, so the rescaled O stays finite; a chunk with no
+    // visible nonzero scale leaves it).  Moving down matters after a chunk with
+    // a few large values: p' = p * 2^(E_x - E_ref) keeps its precision.
     float o_fac = 1.0f;
     if (c == 0) {
       e_ref = e_c;
-    } else if (e_c > e_ref + 4) {
-      const int dd = e_ref - e_c;
-      o_fac = dd > -127 ? __uint_as_float((uint32_t)(127 + dd) << 23) : 0.0f;
-      e_ref = e_c;
+    } else if (e_c > e_ref + 4 || (e_c > 0 && e_c < e_ref - 4)) {
+      const int e_new = max(e_c, e_ref - 90);
+      o_fac = pow2_diff((uint32_t)e_ref, e_new);
+      e_ref = e_new;
     }
-    // exponent of the chunk's V': at most 30 below the reference, so that
-    // p' = p * 2^(E_x - E_ref) cannot underflow while p still counts in l
-    // (groups more than 22 binades below E_x widen to zero: negligible values)
-    const int e_x = max(e_c, e_ref - 30);
-    // V factors 2^(e - E_x) as f16 (0 for tokens past the split or context)
+    // exponent of the chunk's V' (E_x = e_c unless the chunk lies more than 90
+    // binades below the reference)
+    const int e_x = max(e_c, e_ref - 90);
+    // V' holds code * 2^(e - E_x).  As f16 that is exact down to 23 binades
+    // below E_x; a chunk whose visible exponents span more ("wide") widens V'
+    // and writes P' as bf16 instead (fp32's exponent range) and its P.V runs
+    // on bf16 operands.
+    const bool wide = e_c - e_lo > 23;
+    // V factors 2^(e - E_x) as f16 or bf16 bits (0 for tokens past the split or context)
     if (hf == 0) {
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
         const int e = (int)((vsw >> (8 * g4)) & 0xFFu) - e_x;  // <= 0
         const float f = (vok && e >= -126) ? __uint_as_float((uint32_t)(127 + e) << 23) : 0.0f;
-        fac[g4 * kChunk + vt] = __float2half_rn(f);
+        if (wide)
+          reinterpret_cast<uint16_t*>(fac)[g4 * kChunk + vt] = (uint16_t)(__float_as_uint(f) >> 16);
+        else
+          fac[g4 * kChunk + vt] = __float2half_rn(f);
       }
     }
     __syncthreads();  // factors visible
@@ -503,10 +538,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t word = hh ? wv.y : wv.x;
           const uint4 f = fr[pi * 2 + hh];
           uint4 o;
-          o.x = hmul2(e2m1x2_to_f16x2(word, 0), f.x);
-          o.y = hmul2(e2m1x2_to_f16x2(word, 1), f.y);
-          o.z = hmul2(e2m1x2_to_f16x2(word, 2), f.z);
-          o.w = hmul2(e2m1x2_to_f16x2(word, 3), f.w);
+          if (!wide) {
+            o.x = hmul2(e2m1x2_to_f16x2(word, 0), f.x);
+            o.y = hmul2(e2m1x2_to_f16x2(word, 1), f.y);
+            o.z = hmul2(e2m1x2_to_f16x2(word, 2), f.z);
+            o.w = hmul2(e2m1x2_to_f16x2(word, 3), f.w);
+          } else {
+            o.x = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(word, 0)), f.x);
+            o.y = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(word, 1)), f.y);
+            o.z = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(word, 2)), f.z);
+            o.w = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(word, 3)), f.w);
+          }
           *reinterpret_cast<uint4*>(smem + kOffVF + ((d >> 3) * 16 + pi * 2 + hh) * 128 + (d & 7) * 16) = o;
         }
       }
@@ -580,10 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 t = __fadd2_rn(x, sh2);
             const float2 pp = make_float2(ex2(t.x), ex2(t.y));
             ls2[i2 & 1] = __fadd2_rn(ls2[i2 & 1], pp);
-            hw[i2] = pack_f16x2(pp.x, pp.y);
-            const float2 hf2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[i2]));
-            const float2 lo = __fadd2_rn(pp, make_float2(-hf2.x, -hf2.y));
-            lw[i2] = pack_f16x2(lo.x, lo.y);
+            if (!wide) {
+              hw[i2] = pack_f16x2(pp.x, pp.y);
+              const float2 hf2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[i2]));
+              const float2 lo = __fadd2_rn(pp, make_float2(-hf2.x, -hf2.y));
+              lw[i2] = pack_f16x2(lo.x, lo.y);
+            } else {
+              split_bf16x2(pp.x, pp.y, hw[i2], lw[i2]);
+            }
           }
           const int k8 = hf * 8 + q * 4 + o8;  // token octet
           const int off = ((my_r >> 3) * 16 + k8) * 128 + (my_r & 7) * 16;
@@ -630,8 +676,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < kChunk / 16; ++ks) {
         const uint64_t vd = smem_desc(sbase + kOffVF + ks * 256, 2048);
-        mma_f16(tmem + kColO, smem_desc(sbase + kOffP + ks * 256, 2048), vd, (c | ks) != 0);
-        mma_f16(tmem + kColO, smem_desc(sbase + kOffP + kPF + ks * 256, 2048), vd, 1);
+        const uint32_t idesc = wide ? kIdescPVbf16 : kIdescPV;
+        mma_f16(tmem + kColO, smem_desc(sbase + kOffP + ks * 256, 2048), vd, (c | ks) != 0, idesc);
+        mma_f16(tmem + kColO, smem_desc(sbase + kOffP + kPF + ks * 256, 2048), vd, 1, idesc);
       }
       commit(pvdone);
     }
@@ -716,25 +763,40 @@ cudaError_t launch_extend_tc(const DecodeArgs& a, cudaStream_t st) {
   });
   if (!encode) return cudaErrorNotSupported;
   // Each cache as a 2-D tensor of (page, head) blocks: 136 eight-byte elements
-  // per row, row stride 1088 bytes.  Boxes of one row (gather4).
-  ext::Maps maps;
-  const cuuint64_t dims[2] = {(cuuint64_t)ext::kBlk / 8, (cuuint64_t)a.num_pages * a.Hkv};
-  const cuuint64_t strides[1] = {(cuuint64_t)ext::kBlk};
-  const cuuint32_t estr[2] = {1, 1};
-  struct {
-    CUtensorMap* map;
-    const uint8_t* base;
-    cuuint32_t box0;
-  } spec[3] = {{&maps.kcodes, a.k_cache, ext::kCodeBytes / 8},
-               {&maps.kscale, a.k_cache, 8},
-               {&maps.vblock, a.v_cache, ext::kBlk / 8}};
-  for (auto& sp : spec) {
-    const cuuint32_t box[2] = {sp.box0, 1};
-    if (encode(sp.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(sp.base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+  // per row, row stride 1088 bytes.  Boxes of one row (gather4).  As in the
+  // decode launcher, the maps of the caches a host thread used last are kept.
+  struct MapCache {
+    const void* k = nullptr;
+    const void* v = nullptr;
+    cuuint64_t rows = 0;
+    ext::Maps maps;
+  };
+  thread_local MapCache mc;
+  const cuuint64_t rows = (cuuint64_t)a.num_pages * a.Hkv;
+  if (mc.k != a.k_cache || mc.v != a.v_cache || mc.rows != rows) {
+    mc.k = nullptr;
+    const cuuint64_t dims[2] = {(cuuint64_t)ext::kBlk / 8, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ext::kBlk};
+    const cuuint32_t estr[2] = {1, 1};
+    struct {
+      CUtensorMap* map;
+      const uint8_t* base;
+      cuuint32_t box0;
+    } spec[3] = {{&mc.maps.kcodes, a.k_cache, ext::kCodeBytes / 8},
+                 {&mc.maps.kscale, a.k_cache, 8},
+                 {&mc.maps.vblock, a.v_cache, ext::kBlk / 8}};
+    for (auto& sp : spec) {
+      const cuuint32_t box[2] = {sp.box0, 1};
+      if (encode(sp.map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t*>(sp.base), dims, strides, box,
+                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    mc.k = a.k_cache;
+    mc.v = a.v_cache;
+    mc.rows = rows;
   }
+  const ext::Maps& maps = mc.maps;
   static std::atomic<unsigned long long> smem_set{0};
   const cudaError_t e = set_smem_limit_once(ext::extend_fp4_tc_kernel, ext::kSmem, smem_set);
   if (e != cudaSuccess) return e;

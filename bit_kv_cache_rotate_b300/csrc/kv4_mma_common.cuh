@@ -27,9 +27,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 
 // Bounded wait for the phase with the given parity; false on timeout.  The
 // suspend hint lets a waiting warp sleep instead of spinning on issue slots.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// `limit` is the number of tries (a limit of 0 gives up at once: the
+// KV4_DIAG_EXPIRE_FIRST_WAIT test control).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int limit = kSpinLimit) {
   const uint32_t addr = smem_u32(bar);
-  for (int i = 0; i < kSpinLimit; ++i) {
+  for (int i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -62,6 +64,54 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same MMA on bf16 operands: bf16 has the exponent range of fp32, so
+// operands that span more binades than f16 holds keep their value.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// f16x2 -> bf16x2 through fp32; exact for the E2M1 code values (two
+// significant bits).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 l, u;\n\t.reg .f32 fl, fu;\n\tmov.b32 {l, u}, %1;\n\t"
+      "cvt.f32.f16 fl, l;\n\tcvt.f32.f16 fu, u;\n\tcvt.rn.bf16x2.f32 %0, fu, fl;\n\t}"
+      : "=r"(d)
+      : "r"(h));
+  return d;
+}
+
+// A pair x (fp32) as bf16 hi parts and the bf16-rounded remainders: about 16
+// significant bits of x over the whole fp32 exponent range.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(x0, x1);
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xFFFF0000u);
+  lo = pack_bf16x2(x0 - h0, x1 - h1);
+}
+
+// 2^(byte - e) as fp32 for a UE8M0 byte and a reference exponent byte e, the
+// exponent field clamped to [0, 254] (0 gives 0.0: a factor below 2^-126).
+__device__ __forceinline__ float pow2_diff(uint32_t byte, int e) {
+  const int ex = min(254, max(0, 127 + (int)byte - e));
+  return __uint_as_float((uint32_t)ex << 23);
+}
+
+// Nonzero when some byte of x is zero.
+__device__ __forceinline__ uint32_t has_zero_byte(uint32_t x) {
+  return (x - 0x01010101u) & ~x & 0x80808080u;
 }
 
 // One byte of two E2M1 codes -> f16x2 (low nibble -> low half), exact.  The

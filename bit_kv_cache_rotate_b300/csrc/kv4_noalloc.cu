@@ -14,8 +14,12 @@
 
 namespace {
 
-// The fixed scratch.  Every GPU that loads libkv4 holds these bytes until the
-// process exits.
+// The fixed scratch.  It is part of this file's device module: the CUDA
+// runtime reserves its bytes on a device when it loads the module there, and
+// they stay reserved until the process exits.  Under CUDA's default lazy
+// module loading the load happens at the first symbol lookup below, that is
+// the first call of the entry point on that device; with eager loading
+// (CUDA_MODULE_LOADING=EAGER) it happens when the context is created.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KV4_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -48,7 +52,13 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     const int32_t* context_lens, int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
     int head_dim, int page_size, int max_pages_per_seq, int num_pages, float softmax_scale,
     int num_splits, float* out, int32_t* dev_error, kv4_stream_t stream) {
-  if (batch == 0) return KV4_OK;
+  if (batch == 0) {
+    // nothing to compute: the regular entry point validates the rest of the
+    // shape and returns without launching
+    return kv4_decode_attention(q, k_cache, v_cache, block_tables, context_lens, batch, q_per_seq,
+                                num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
+                                num_pages, softmax_scale, num_splits, nullptr, 0, out, dev_error, stream);
+  }
   if (num_splits < 0) return KV4_ERR_INVALID_ARG;
   int S = num_splits ? num_splits
                      : kv4_decode_auto_splits(batch, q_per_seq, num_q_heads, num_kv_heads, head_dim,

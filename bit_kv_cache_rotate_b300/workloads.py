@@ -7,7 +7,9 @@ and the CPU oracle can both be fed from it.
 The shapes follow the long-context agentic serving described on the
 "UltraQuant on AMD Instinct" page (section "Agentic serving / workload and
 setup": long shared prefixes, prefix caching hit rate 91-95 %, 262K context;
-section "Throughput-latency trade-off": 3-position MTP verify) and the MLA
+section "Throughput-latency trade-off": 3-position MTP verify, with fused
+multi-token decode as future work; the 6-token EAGLE verify of the OneNexus
+"GLM-5.3-Flash MXFP4" page) and the MLA
 latent row of the GLM serving note (512 values per token, no RoPE half).
 The page replays an InferenceX agentic trace that is not available here;
 these seeded generators stand in for it.
@@ -61,6 +63,9 @@ CONFIGS = {
     # MTP verify + agentic traffic: ragged 16K..128K contexts, 93 % shared prefix pages, T = 3.
     "verify_agentic": Config("verify_agentic", 32, 3, 64, 8, 128, 16, ("uniform", 16384, 131072),
                              outliers="pct2x16", shared_prefix=0.93, seed=1239),
+    # Longer verify block (EAGLE-style 6-token speculation): the same traffic, T = 6.
+    "verify6_agentic": Config("verify6_agentic", 32, 6, 64, 8, 128, 16, ("uniform", 16384, 131072),
+                              outliers="pct2x16", shared_prefix=0.93, seed=1241),
     # Extend step: a 512-token chunk of new prompt per sequence over a 32K cached
     # context (the chunk included), causal among the new tokens.
     "extend_b4_ctx32k_t512": Config("extend_b4_ctx32k_t512", 4, 512, 64, 8, 128, 16, ("fixed", 32768),

@@ -35,8 +35,12 @@
  *   - Entry points are thread-safe.  Their only process-wide state is set up
  *     once and never changes results: each kernel's raised shared-memory
  *     limit (per device), the driver's tensor-map encoder (looked up once),
- *     and for kv4_decode_attention_noalloc the address of its scratch array
- *     (per device; that array's ordering rule is stated there).
+ *     per host thread the tensor maps (address and sizes) of the caches that
+ *     thread decoded last, re-encoded whenever a cache pointer or size
+ *     differs, and for kv4_decode_attention_noalloc the address of its
+ *     scratch array (per device; that array's ordering rule is stated there).
+ *     Nothing reads the environment; the kernel choice depends on the shape
+ *     alone (kv4_decode_attention_select makes it explicit).
  *
  * Cache layout (one block per (page, kv head), blocks page-major:
  * block index = page * num_kv_heads + head, block bytes = P*D/2 + P*D/32):
@@ -83,7 +87,8 @@ typedef enum {
 #define KV4_MAX_Q_PER_SEQ 4096
 
 #define KV4_DEVERR_PAGE 1      /* block_tables entry outside [0, num_pages) */
-#define KV4_DEVERR_CONTEXT 2   /* context_lens[b] outside [q_per_seq, max_pages*page_size] */
+#define KV4_DEVERR_CONTEXT 2   /* context_lens[b] outside [q_per_seq, max_pages*page_size]
+                                  ([0, ...] for kv4_decode_partials_prefix) */
 #define KV4_DEVERR_SLOT 4      /* slot_mapping entry outside the cache */
 #define KV4_DEVERR_TIMEOUT 8   /* a bounded wait for streamed cache data gave up */
 
@@ -169,6 +174,30 @@ kv4_status kv4_decode_partials(const void* q, const uint8_t* k_cache, const uint
                                float softmax_scale, int num_splits, void* workspace,
                                size_t workspace_bytes, int32_t* dev_error, kv4_stream_t stream);
 
+/* The split stage over a leading share of each sequence's cache, for one
+ * long context split across devices ("GLM-5.3-Flash on MI300X": sharding the
+ * KV cache instead of replicating it is what frees capacity for long
+ * contexts).  A sequence's pages are cut into consecutive shares, one per
+ * device; the device that holds the newest tokens (the q_per_seq query
+ * positions and everything after the other shares) calls
+ * kv4_decode_partials on its share, every other device calls this entry point
+ * on its own.  Here every cached token precedes the query positions, so all of
+ * them are visible to every position (no causal mask); context_lens[b] is the
+ * share's token count and may be 0 (an empty share writes empty partials:
+ * lse = -inf).  Arguments, layout and errors are those of kv4_decode_partials.
+ * The partials of all shares, gathered into one device's memory and
+ * concatenated along the split axis (partial_o [B][T][Hq][S_total][D],
+ * partial_lse [B][T][Hq][S_total]), merge with kv4_split_combine into the
+ * attention over the whole sequence: the log-sum-exp merge is exact whatever
+ * the order and grouping of the splits. */
+kv4_status kv4_decode_partials_prefix(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int page_size, int max_pages_per_seq,
+                                      int num_pages, float softmax_scale, int num_splits,
+                                      void* workspace, size_t workspace_bytes, int32_t* dev_error,
+                                      kv4_stream_t stream);
+
 /* Decode attention for callers that cannot allocate device memory.
  * The paper has no counterpart to this entry point; it exists for callers
  * such as operator plugins that the host framework hands only input and
@@ -177,14 +206,24 @@ kv4_status kv4_decode_partials(const void* q, const uint8_t* k_cache, const uint
  * Arguments and results are those of kv4_decode_attention without the
  * workspace: the split partials live in a fixed array of
  * KV4_NOALLOC_SCRATCH_BYTES bytes in device global memory that libkv4
- * declares itself (every GPU that loads the library keeps it until exit).
- * The call allocates nothing and calls no allocating routine.
+ * declares itself.  The call itself allocates nothing and calls no
+ * allocating routine (no cudaMalloc, no memory-pool or library allocator).
+ *   - The array is reserved on a device when the CUDA runtime loads the
+ *     library's module that holds it there.  Under CUDA's default lazy module
+ *     loading that is the first call of this entry point on the device (its
+ *     address lookup loads the module), so that first call can fail with
+ *     KV4_ERR_CUDA if the device has no 16 MiB left; with
+ *     CUDA_MODULE_LOADING=EAGER it is reserved when the context is created.
+ *     Make the first call during set-up, before a memory pool takes the
+ *     device's free memory; the array then stays reserved until the process
+ *     exits and later calls reserve nothing.
  *   - num_splits = 0 picks kv4_decode_auto_splits, lowered if needed to the
  *     largest count whose partials (kv4_decode_workspace_bytes) fit.  An
  *     explicit num_splits whose partials do not fit, or a request that does
  *     not fit even with one split per sequence, returns KV4_ERR_INVALID_ARG
- *     before anything is launched.
- *   - The first call on each device looks up the array's device address
+ *     before anything is launched.  batch = 0 is validated like
+ *     kv4_decode_attention and launches nothing.
+ *   - The first call on each device also looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins.
  *   - All calls share the array, which keeps what the last call wrote.
@@ -200,6 +239,42 @@ kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
                                         int page_size, int max_pages_per_seq, int num_pages,
                                         float softmax_scale, int num_splits, float* out,
                                         int32_t* dev_error, kv4_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * Kernel choice and test controls (diagnostics).
+ *
+ * kv4_decode_attention picks the split kernel from the shape alone.  This
+ * entry point is the same call with that choice made explicit, for tests and
+ * measurements that compare the kernels on one input.  Every kernel computes
+ * the same attention (the results differ by accumulation order, well inside
+ * the 2e-3 parity tolerance); a kernel that does not serve the shape returns
+ * KV4_ERR_UNSUPPORTED before anything is launched.  No global state: the
+ * choice applies to this call only.
+ * --------------------------------------------------------------------- */
+#define KV4_KERNEL_AUTO 0      /* what kv4_decode_attention picks */
+#define KV4_KERNEL_WARP_MMA 1  /* warp-MMA kernel: head_dim 128, <= 8 query heads per kv head;
+                                  up to 24 rows per CTA, more rows as position tiles */
+#define KV4_KERNEL_EXTEND 2    /* tcgen05 extend kernel: head_dim 128, G in {1,2,4,8}, > 24 rows */
+#define KV4_KERNEL_LATENT 3    /* latent (MLA) kernel: head_dim 512, K = V, <= 16 rows */
+#define KV4_KERNEL_GENERAL 4   /* CUDA-core kernel: every shape within the documented row limits */
+
+/* Test controls (bits of diag_flags; 0 in normal use).
+ * KV4_DIAG_EXPIRE_FIRST_WAIT: the first bounded wait of every warp that streams
+ *   cache data gives up without trying, as a wait that ran out would.  The
+ *   kernel then sets KV4_DEVERR_TIMEOUT in *dev_error, waits (bounded) for
+ *   the copies it issued, and returns; the output is not meaningful.  It
+ *   exercises the timeout path without a fault or a hang; kernels without
+ *   streamed waits (the general kernel) ignore it. */
+#define KV4_DIAG_EXPIRE_FIRST_WAIT 1
+
+kv4_status kv4_decode_attention_select(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens,
+                                       int batch, int q_per_seq, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int page_size, int max_pages_per_seq,
+                                       int num_pages, float softmax_scale, int num_splits,
+                                       void* workspace, size_t workspace_bytes, float* out,
+                                       int32_t* dev_error, int kernel, int diag_flags,
+                                       kv4_stream_t stream);
 
 /* Log-sum-exp merge of split partials, then the inverse rotation:
  *   lse = log sum_s exp(lse_s);  O = sum_s exp(lse_s - lse) O_s;  out = H_D O.

@@ -144,3 +144,33 @@ def test_noalloc_rejects_before_touching_the_device(lib):
     assert na(fake, fake, fake, fake, fake, B, T, Hq, Hkv, D, 16, 4, 8, 0.1, -1, fake, None, None) == \
         kv4.KV4_ERR_INVALID_ARG
     assert na(fake, fake, fake, fake, fake, 0, T, Hq, Hkv, D, 16, 4, 8, 0.1, 0, fake, None, None) == kv4.KV4_OK
+    # batch 0 is validated like kv4_decode_attention: a bad shape is still refused
+    assert na(fake, fake, fake, fake, fake, 0, T, Hq, Hkv, 96, 16, 4, 8, 0.1, 0, fake, None, None) == \
+        kv4.KV4_ERR_UNSUPPORTED
+    assert na(fake, fake, fake, fake, fake, 0, T, 63, Hkv, D, 16, 4, 8, 0.1, 0, fake, None, None) == \
+        kv4.KV4_ERR_INVALID_ARG
+
+
+def test_kernel_choice_is_validated_before_launch(lib):
+    """kv4_decode_attention_select: an unknown kernel id is an invalid argument,
+    a kernel that does not serve the shape is unsupported; both return before
+    any launch."""
+    P = ctypes.c_void_p
+    fake = P(4096)
+    ws = P(4096 * 256)
+    sel = lib.kv4_decode_attention_select
+
+    def args(kernel, T=1, Hq=8, Hkv=2, D=128, v=fake, diag=0):
+        return [fake, fake, v, fake, fake, 2, T, Hq, Hkv, D, 16, 4, 8, 0.1, 1, ws, 1 << 24, fake, None,
+                kernel, diag, None]
+
+    assert sel(*args(99)) == kv4.KV4_ERR_INVALID_ARG
+    assert sel(*args(-1)) == kv4.KV4_ERR_INVALID_ARG
+    assert sel(*args(kv4.KV4_KERNEL_LATENT)) == kv4.KV4_ERR_UNSUPPORTED        # not a latent cache
+    assert sel(*args(kv4.KV4_KERNEL_EXTEND)) == kv4.KV4_ERR_UNSUPPORTED        # 4 rows: not an extend tile
+    assert sel(*args(kv4.KV4_KERNEL_WARP_MMA, D=64)) == kv4.KV4_ERR_UNSUPPORTED  # head_dim 64
+    assert sel(*args(kv4.KV4_KERNEL_GENERAL, T=40, Hq=16)) == kv4.KV4_ERR_UNSUPPORTED  # 320 rows
+    # the env switches of earlier versions are gone: nothing in the library reads the environment
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--undefined-only", kv4.LIB_PATH], capture_output=True, text=True).stdout
+    assert "getenv" not in out

@@ -5,7 +5,6 @@ CTAs; each CTA is checked through the whole output against the oracle's fp64
 attention (max abs error 2e-3), across tile boundaries, ragged contexts,
 split counts, GQA groups and the pure-prefill case (context == chunk)."""
 import dataclasses
-import os
 
 import numpy as np
 import pytest
@@ -28,7 +27,7 @@ def _cfg(T, ctx, batch=2, Hq=64, Hkv=8, seed=None):
                                seed=c.seed if seed is None else seed)
 
 
-def _run(cfg, num_splits=0, fp8=False):
+def _run(cfg, num_splits=0, fp8=False, kernel=0):
     lay = W.make_layout(cfg)
     k, v, slots = all_tokens(cfg, lay)
     q = W.queries(cfg)
@@ -37,8 +36,8 @@ def _run(cfg, num_splits=0, fp8=False):
     if not fp8:
         okc, ovc = oracle_caches(cfg, lay, k, v, slots)
         gkc, gvc = gpu_caches(kv4, cfg, lay, k, v, slots)
-        out = kv4.kv4_decode_attention(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
-                                       cfg.softmax_scale, num_splits=num_splits)
+        out = kv4.kv4_decode_attention_select(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
+                                              cfg.softmax_scale, kernel, num_splits=num_splits)
         torch.cuda.synchronize()
         ref = oracle.decode_attention(q, okc, ovc, otab, lay.context_lens, cfg.num_kv_heads, cfg.page_size,
                                       lay.num_pages, cfg.softmax_scale)
@@ -97,11 +96,10 @@ def test_extend_fp8_comparator():
 
 
 @pytest.mark.parametrize("warp", [False, True])
-def test_extend_both_kernels(warp, monkeypatch):
+def test_extend_both_kernels(warp):
     """G = 8 and 4 on the tcgen05 extend kernel (default) and on the warp-MMA
-    kernel's position tiles (KV4_EXTEND_WARPMMA=1)."""
-    if warp:
-        monkeypatch.setenv("KV4_EXTEND_WARPMMA", "1")
+    kernel's position tiles (KV4_KERNEL_WARP_MMA)."""
+    kernel = kv4.KV4_KERNEL_WARP_MMA if warp else kv4.KV4_KERNEL_AUTO
     for Hq, Hkv, T, ctx in [(64, 8, 48, ("uniform", 300, 1100)), (16, 4, 130, ("uniform", 200, 700))]:
-        err = _run(_cfg(T, ctx, Hq=Hq, Hkv=Hkv))
+        err = _run(_cfg(T, ctx, Hq=Hq, Hkv=Hkv), kernel=kernel)
         assert err <= TOL, (warp, Hq, Hkv, T, err)

@@ -4,8 +4,10 @@ decode with the automatic split count) runs on the GPU; sampled (sequence, kv
 head) pairs are recomputed one by one by the oracle -- every cached K/V block
 of the sample bit-exact, its attention rows within 2e-3.  Workloads covered:
 batch 32 at a 32K context (4-bit path and the FP8 comparator on the same
-inputs) and at 8K, the 512-wide MLA latent cache at batch 8 and a 96K context, the
-3-position verify step over ragged 16K-128K contexts with a 93 % shared prefix,
+inputs), at 16K, and at 8K (there every K and V vector of the cache is
+checked, not a sample), the 512-wide MLA latent cache at batch 8 and a 96K context, the
+3-position verify step over ragged 16K-128K contexts with a 93 % shared prefix
+(every token the step appends checked bit-exact),
 and the extend step (batch 4, a 512-token chunk over a 32K context) on both
 extend kernels at sampled chunk positions."""
 import numpy as np
@@ -167,6 +169,34 @@ def test_fullsize_8k_sampled_parity(fullsize_8k, b, h):
     _check_sample(cfg, wl, out, b, h)
 
 
+def test_fullsize_8k_every_vector_bit_exact(fullsize_8k):
+    """Every K and V vector of the 8K step (32 sequences x 8192 tokens x 8 kv
+    heads, the step's appended tokens included): the whole GPU cache equal to
+    the oracle's, byte for byte.  Every page of this workload is full, so
+    every byte of both caches is written."""
+    from _harness import all_tokens, oracle_caches
+    cfg, wl, _ = fullsize_8k
+    lay = wl.lay
+    assert (lay.context_lens % cfg.page_size == 0).all()
+    k, v, slots = all_tokens(cfg, lay)
+    okc, ovc = oracle_caches(cfg, lay, k, v, slots)
+    for name, g, o in (("K", wl.kc, okc), ("V", wl.vc, ovc)):
+        diff = np.flatnonzero(g.cpu().numpy() != o)
+        assert diff.size == 0, f"{name} cache differs at {diff[:8]} ({diff.size} bytes)"
+
+
+# ---- batch 32 at a 16K context: the middle of the context sweep
+@pytest.fixture(scope="module")
+def fullsize_16k():
+    return _bench_step("b32_ctx16k")
+
+
+@pytest.mark.parametrize("b,h", [(2, 4), (19, 0), (31, 7)])
+def test_fullsize_16k_sampled_parity(fullsize_16k, b, h):
+    cfg, wl, out = fullsize_16k
+    _check_sample(cfg, wl, out, b, h)
+
+
 # ---- MLA latent cache at full size: batch 8, a 98304-token context, one 512-wide latent head
 @pytest.fixture(scope="module")
 def fullsize_mla():
@@ -193,6 +223,44 @@ def _verify_samples():
     return [(int(np.argmax(lens)), 7), (int(np.argmin(lens)), 2), (13, 4)]
 
 
+def test_fullsize_verify_every_new_token_bit_exact(fullsize_verify):
+    """Every token the verify step appends (3 per sequence, 32 sequences, 8 kv
+    heads, K and V): the bits each one writes into its page equal the oracle's.
+    The written bits are found by appending the page's new tokens into two
+    oracle blocks that start all-zero and all-one."""
+    cfg, wl, _, _ = fullsize_verify
+    lay, P, D, T, Hkv = wl.lay, cfg.page_size, cfg.head_dim, cfg.q_per_seq, cfg.num_kv_heads
+    bb = oracle.block_bytes(P, D)
+    gk, gv = wl.kc.cpu().numpy(), wl.vc.cpu().numpy()
+    checked = 0
+    for b in range(cfg.batch):
+        L = int(lay.context_lens[b])
+        k, v = W.private_tokens(cfg, lay, b)
+        k, v = k[-T:], v[-T:]
+        pos = np.arange(L - T, L)
+        for page_idx in np.unique(pos // P):
+            sel = np.flatnonzero(pos // P == page_idx)
+            phys = int(lay.block_tables[b, page_idx])
+            for h in range(Hkv):
+                kh = k[sel, h:h + 1].contiguous()
+                vh = v[sel, h:h + 1].contiguous()
+                offs = (pos[sel] % P).astype(np.int32)
+                blk = []
+                for fill in (0x00, 0xFF):
+                    kb = np.full(bb, fill, np.uint8)
+                    vb = np.full(bb, fill, np.uint8)
+                    assert oracle.append_quantize(kh, vh, offs, kb, vb, 1, P) == oracle.OK
+                    blk.append((kb, vb))
+                (k0, v0), (k1, v1) = blk
+                base = (phys * Hkv + h) * bb
+                for g, o0, o1, part in ((gk, k0, k1, "K"), (gv, v0, v1, "V")):
+                    mask = ~(o0 ^ o1)  # the bits the new tokens write
+                    assert not np.any((g[base:base + bb] ^ o0) & mask), \
+                        f"sequence {b}, kv head {h}, page {page_idx}: {part} bits of the new tokens differ"
+                checked += len(sel)
+    assert checked == cfg.batch * T * Hkv
+
+
 @pytest.mark.parametrize("b,h", _verify_samples())
 def test_fullsize_verify_sampled_parity(fullsize_verify, b, h):
     """The shortest and the longest sequence plus one more: their shared-prefix
@@ -202,25 +270,39 @@ def test_fullsize_verify_sampled_parity(fullsize_verify, b, h):
     _check_sample(cfg, wl, out, b, h, chain=chain)
 
 
+# ---- 6-position verify at full size: the same traffic with T = 6 (48 rows per kv head)
+@pytest.fixture(scope="module")
+def fullsize_verify6():
+    cfg, wl, out = _bench_step("verify6_agentic")
+    chain = W.chain_tokens(cfg, wl.lay, 0, int(wl.lay.chain.size) * cfg.page_size)
+    return cfg, wl, out, chain
+
+
+def _verify6_samples():
+    lens = W.make_layout(W.CONFIGS["verify6_agentic"]).context_lens
+    return [(int(np.argmax(lens)), 3), (int(np.argmin(lens)), 6)]
+
+
+@pytest.mark.parametrize("b,h", _verify6_samples())
+def test_fullsize_verify6_sampled_parity(fullsize_verify6, b, h):
+    cfg, wl, out, chain = fullsize_verify6
+    _check_sample(cfg, wl, out, b, h, chain=chain)
+
+
 # ---- extend step at full size: batch 4, a 512-token chunk over a 32K context
 EXT_SAMPLES = [(0, 5, (0, 300, 511)), (3, 2, (17, 511))]  # (sequence, kv head, positions)
 
 
 @pytest.fixture(scope="module", params=["tcgen05", "warp"])
 def fullsize_extend(request):
-    import os
     import bench
-    if request.param == "warp":
-        os.environ["KV4_EXTEND_WARPMMA"] = "1"
-    try:
-        cfg = W.CONFIGS["extend_b4_ctx32k_t512"]
-        wl = bench.Workload(cfg, kv4, with_fp8=False)
-        kv4.kv4_append_quantize(wl.new_k, wl.new_v, wl.new_slots, wl.kc, wl.vc, wl.lay.num_pages)
-        out = kv4.kv4_decode_attention(wl.q, wl.kc, wl.vc, wl.tab, wl.lens, cfg.num_kv_heads, wl.lay.num_pages,
-                                       cfg.softmax_scale, num_splits=wl.S, workspace_buf=wl.ws)
-        torch.cuda.synchronize()
-    finally:
-        os.environ.pop("KV4_EXTEND_WARPMMA", None)
+    kernel = kv4.KV4_KERNEL_WARP_MMA if request.param == "warp" else kv4.KV4_KERNEL_AUTO
+    cfg = W.CONFIGS["extend_b4_ctx32k_t512"]
+    wl = bench.Workload(cfg, kv4, with_fp8=False)
+    kv4.kv4_append_quantize(wl.new_k, wl.new_v, wl.new_slots, wl.kc, wl.vc, wl.lay.num_pages)
+    out = kv4.kv4_decode_attention_select(wl.q, wl.kc, wl.vc, wl.tab, wl.lens, cfg.num_kv_heads, wl.lay.num_pages,
+                                          cfg.softmax_scale, kernel, num_splits=wl.S, workspace_buf=wl.ws)
+    torch.cuda.synchronize()
     return cfg, wl, out.cpu().numpy().astype(np.float64)
 
 

@@ -23,6 +23,7 @@ SMALL = {
     "b32_small": W.scaled(W.CONFIGS["b32_ctx8k"], batch=3, ctx=("fixed", 1000)),
     "mla_small": W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=2, ctx=("fixed", 777)),
     "verify_small": W.scaled(W.CONFIGS["verify_agentic"], batch=4, ctx=("uniform", 300, 1500)),
+    "verify6_small": W.scaled(W.CONFIGS["verify6_agentic"], batch=4, ctx=("uniform", 300, 1500)),
 }
 
 

@@ -29,28 +29,23 @@ kv4 = pytest.importorskip("bit_kv_cache_rotate_b300")
 _B32 = W.CONFIGS["b32_ctx8k"]
 _EXT = W.CONFIGS["extend_b4_ctx32k_t512"]
 
-# name -> (config, environment switch or None)
+# name -> (config, kernel choice)
 CASES = {
-    "decode": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), None),
-    "decode_tcgen05": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), "KV4_DECODE_TCGEN05"),
-    "verify": (W.scaled(W.CONFIGS["verify_agentic"], batch=4, ctx=("uniform", 300, 1500)), None),
-    "mla": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=("uniform", 17, 900)), None),
-    "extend_tcgen05": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 100, 700)), q_per_seq=40),
-                       None),
-    "extend_warp": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 100, 700)), q_per_seq=40),
-                    "KV4_EXTEND_WARPMMA"),
-    "general_g10": (dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), num_q_heads=80),
-                    None),
-    "general_d64": (dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), head_dim=64), None),
+    "decode": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 0),
+    "decode_general": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 4),
+    "verify": (W.scaled(W.CONFIGS["verify_agentic"], batch=4, ctx=("uniform", 300, 1500)), 0),
+    "mla": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=("uniform", 17, 900)), 0),
+    "extend_tcgen05": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 100, 700)), q_per_seq=40), 0),
+    "extend_warp": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 100, 700)), q_per_seq=40), 1),
+    "general_g10": (dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), num_q_heads=80), 0),
+    "general_d64": (dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), head_dim=64), 0),
 }
 
 
 @pytest.mark.parametrize("fill", [0xFF, 0xC3])
 @pytest.mark.parametrize("name", list(CASES))
-def test_4bit_attention_ignores_unwritten_slots(name, fill, monkeypatch):
-    cfg, env = CASES[name]
-    if env:
-        monkeypatch.setenv(env, "1")
+def test_4bit_attention_ignores_unwritten_slots(name, fill):
+    cfg, kernel = CASES[name]
     lay = W.make_layout(cfg)
     assert (lay.context_lens % cfg.page_size != 0).any(), "the case needs partly filled pages"
     k, v, slots = all_tokens(cfg, lay)
@@ -60,8 +55,8 @@ def test_4bit_attention_ignores_unwritten_slots(name, fill, monkeypatch):
     tab, lens = gpu_tables(lay)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for S in (1, 3):
-        out = kv4.kv4_decode_attention(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
-                                       cfg.softmax_scale, num_splits=S, dev_error=err)
+        out = kv4.kv4_decode_attention_select(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
+                                              cfg.softmax_scale, kernel, num_splits=S, dev_error=err)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
         got = out.cpu().numpy().astype(np.float64)

@@ -76,3 +76,43 @@ def test_noalloc_rejects_partials_beyond_its_scratch():
     torch.cuda.synchronize()
     assert st == kv4.KV4_ERR_INVALID_ARG
     assert (out == 7.0).all()  # nothing was launched
+
+
+def test_noalloc_lowers_an_automatic_split_count_that_does_not_fit():
+    """head_dim 256, 24 query rows per kv head, 8 sequences: the automatic split
+    count (130) needs about 24 MiB of partials, more than the fixed array holds.
+    With num_splits = 0 the entry point lowers the count until they fit and
+    must still match the workspace entry point (which keeps the 130 splits)."""
+    import dataclasses
+    cfg = dataclasses.replace(W.CONFIGS["b32_ctx8k"], name="d256_g24", batch=8, ctx=("fixed", 8320),
+                              num_q_heads=24, num_kv_heads=1, head_dim=256)
+    lay, kc, vc, tab, lens = _cache(cfg)
+    S = kv4.kv4_decode_auto_splits(cfg.batch, 1, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim,
+                                   cfg.page_size, tab.shape[1])
+    assert kv4.kv4_decode_workspace_bytes(cfg.batch, 1, cfg.num_q_heads, cfg.head_dim, S) > 16 << 20
+    q = W.queries(cfg).cuda()
+    want = kv4.kv4_decode_attention(q, kc, vc, tab, lens, cfg.num_kv_heads, lay.num_pages, cfg.softmax_scale)
+    got = torch.full_like(want, float("nan"))
+    st = _noalloc_c(q, kc, vc, tab, lens, cfg, lay, 0, got)
+    torch.cuda.synchronize()
+    assert st == kv4.KV4_OK
+    assert torch.isfinite(got).all()
+    assert (got - want).abs().max().item() <= TOL
+
+
+def test_noalloc_reserves_no_memory_after_its_first_call():
+    """The fixed array is reserved when the library's module holding it loads on
+    the device (at the first call, under CUDA's lazy module loading); from then
+    on calls leave the device's free memory unchanged."""
+    cfg = W.scaled(W.CONFIGS["b32_ctx8k"], batch=3, ctx=("fixed", 1000))
+    lay, kc, vc, tab, lens = _cache(cfg)
+    q = W.queries(cfg).cuda()
+    out = torch.empty((cfg.batch, 1, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device="cuda")
+    assert _noalloc_c(q, kc, vc, tab, lens, cfg, lay, 0, out) == kv4.KV4_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert _noalloc_c(q, kc, vc, tab, lens, cfg, lay, 0, out) == kv4.KV4_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory moved by {free0 - free1} bytes"
