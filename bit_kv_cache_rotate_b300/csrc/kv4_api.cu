@@ -202,16 +202,28 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   // latent kernel, head_dim 128 with up to 8 query heads per kv head on the
   // warp-MMA kernel, everything else on the general kernel.  An explicit
   // choice (kv4_decode_attention_select) must serve the shape.
+  const bool ok_tc = !fp8 && kv4::tc_path_supported(D, G, T, latent);
   const bool ok_ext = !fp8 && kv4::extend_tc_supported(D, G, T, latent);
   const bool ok_mla = !fp8 && kv4::mla_path_supported(D, G, T, latent);
   const bool ok_warp = fp8 ? kv4::fp8_fast_path_supported(D, G, T) : kv4::fast_path_supported(D, G, T, latent);
   const bool ok_gen = T * G <= kv4::ref_max_rows(D);
+  // The extend kernel's tile is 128 query rows; a block of a few positions
+  // (a 6-token verify: 48 rows) leaves most of it idle and runs slower than the
+  // warp-MMA kernel's position tiles reading the pages once per 24 rows (L2
+  // serves the repeats), so automatic choice sends only blocks above 96 rows
+  // (four tiles of 24) to the extend kernel.
   int k = kernel;
   if (k == KV4_KERNEL_AUTO)
-    k = ok_ext ? KV4_KERNEL_EXTEND : ok_mla ? KV4_KERNEL_LATENT : ok_warp ? KV4_KERNEL_WARP_MMA
-                                                                           : KV4_KERNEL_GENERAL;
+    k = (ok_ext && T * G > 4 * kv4::kTileRows) ? KV4_KERNEL_EXTEND
+        : ok_mla                               ? KV4_KERNEL_LATENT
+        : ok_warp                              ? KV4_KERNEL_WARP_MMA
+                                               : KV4_KERNEL_GENERAL;
   cudaError_t e;
   switch (k) {
+    case KV4_KERNEL_TCGEN05:
+      if (!ok_tc) return KV4_ERR_UNSUPPORTED;
+      e = kv4::launch_decode_tc(a, st);
+      break;
     case KV4_KERNEL_EXTEND:
       if (!ok_ext) return KV4_ERR_UNSUPPORTED;
       e = kv4::launch_extend_tc(a, st);

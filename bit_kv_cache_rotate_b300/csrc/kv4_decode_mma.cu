@@ -369,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     const bool edge = nv < kPagesPerChunk || (pg + kPagesPerChunk) * kPage > min_limit;
 
     // ---- scale tables: lane -> page lane>>3, token pair lane&7
-    uint32_t eold, enew = 0;
-    bool slow;
+    uint32_t eold;
+    bool under;  // this lane holds a visible V scale below the f16 window
     {
       const int pp = lane >> 3, pr = lane & 7, tk = 2 * pr;
       const int pos = (pg + pp) * kPage + tk;
@@ -420,30 +420,19 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
       const uint32_t a0 = __vsubus4(0x16161616u, __vsubus4(lim, ok0 ? v0 : lim));
       const uint32_t a1 = __vsubus4(0x16161616u, __vsubus4(lim, ok1 ? v1 : lim));
       // A zero field is a V scale more than 14 binades below the reference
-      // (or a zero byte: an all-zero group); f16 cannot carry that factor, so
-      // the chunk takes the bf16 path below with a reference re-taken from the
-      // chunk itself: each group's largest V exponent of the chunk (at most 90
-      // binades below the old one, so the rescaled O stays finite).  Groups
-      // with no visible token keep their reference.
-      slow = __any_sync(0xffffffffu, (has_zero_byte(a0) | has_zero_byte(a1)) != 0u);
-      if (slow) {
-        uint32_t cm = __vmaxu4(v0, v1);
-#pragma unroll
-        for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
-        const uint32_t none = __vcmpeq4(cm, 0u);
-        enew = (__vmaxu4(cm, __vsubus4(eold, 0x5A5A5A5Au)) & ~none) | (eold & none);
-      } else {
-        uint4 vp;
-        vp.x = __byte_perm(__byte_perm(a0, a1, 0x0040), 0, 0x5140) << 10;
-        vp.y = __byte_perm(__byte_perm(a0, a1, 0x0051), 0, 0x5140) << 10;
-        vp.z = __byte_perm(__byte_perm(a0, a1, 0x0062), 0, 0x5140) << 10;
-        vp.w = __byte_perm(__byte_perm(a0, a1, 0x0073), 0, 0x5140) << 10;
-        uint32_t* vt = vtab + pp * (kVTabPage / 4) + pr;
-        vt[0] = vp.x;
-        vt[8] = vp.y;
-        vt[16] = vp.z;
-        vt[24] = vp.w;
-      }
+      // (or a zero byte: an all-zero group): f16 cannot carry that factor, and
+      // the chunk's P.V takes the bf16 path below (the vote waits until then).
+      under = (has_zero_byte(a0) | has_zero_byte(a1)) != 0u;
+      uint4 vp;
+      vp.x = __byte_perm(__byte_perm(a0, a1, 0x0040), 0, 0x5140) << 10;
+      vp.y = __byte_perm(__byte_perm(a0, a1, 0x0051), 0, 0x5140) << 10;
+      vp.z = __byte_perm(__byte_perm(a0, a1, 0x0062), 0, 0x5140) << 10;
+      vp.w = __byte_perm(__byte_perm(a0, a1, 0x0073), 0, 0x5140) << 10;
+      uint32_t* vt = vtab + pp * (kVTabPage / 4) + pr;
+      vt[0] = vp.x;
+      vt[8] = vp.y;
+      vt[16] = vp.z;
+      vt[24] = vp.w;
       __syncwarp();
     }
 
@@ -555,25 +544,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
         a1[rb] = __shfl_sync(0xffffffffu, alpha[rb], 8 * t + 4);
         any_a |= a0[rb] != 1.0f || a1[rb] != 1.0f;
       }
-      if (slow) {
-        // the reference moves to enew, up or down: factor 2^(Eold - Enew)
-#pragma unroll
-        for (int G4 = 0; G4 < 4; ++G4) {
-          const float f = pow2_diff((eold >> (8 * G4)) & 0xFFu, (int)((enew >> (8 * G4)) & 0xFFu));
-#pragma unroll
-          for (int rb = 0; rb < RB; ++rb) {
-            const float f0 = f * a0[rb], f1 = f * a1[rb];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              o[rb][2 * G4 + jj][0] *= f0;
-              o[rb][2 * G4 + jj][1] *= f1;
-              o[rb][2 * G4 + jj][2] *= f0;
-              o[rb][2 * G4 + jj][3] *= f1;
-            }
-          }
-        }
-        eref = enew;
-      } else if (__any_sync(0xffffffffu, eold != eref || any_a)) {
+      if (__any_sync(0xffffffffu, eold != eref || any_a)) {
         const uint32_t dl = __vsubus4(eref, eold);  // Enew - Eold per group
 #pragma unroll
         for (int G4 = 0; G4 < 4; ++G4) {
@@ -600,8 +571,37 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     // some p of the step (any row, any page) exceeds 2^-8; below that the f16
     // rounding of p alone stays under 2^-20 per token.
     const uint8_t* vbase = stg + kPagesPerChunk * kBlkStride + t * kVStride;
-    if (slow) {
-      pv_bf16<RB>(o, p, vbase, enew, g);
+    if (__any_sync(0xffffffffu, under)) {
+      // The reference is re-taken from the chunk itself: each group's largest
+      // visible V exponent (at most 90 binades below the current one, so the
+      // rescaled O stays finite; groups with no visible token keep theirs).
+      // It moves up or down, and O is rescaled by 2^(Eref - Enew).
+      const int pp = lane >> 3, tk = 2 * (lane & 7);
+      const int pos = (pg + pp) * kPage + tk;
+      uint32_t v0 = 0, v1 = 0;
+      if (pp < nv) {
+        const uint2 vv =
+            *reinterpret_cast<const uint2*>(stg + kPagesPerChunk * kBlkStride + pp * kVStride + kCodeBytes + tk * 4);
+        if (pos < L) v0 = vv.x;
+        if (pos + 1 < L) v1 = vv.y;
+      }
+      uint32_t cm = __vmaxu4(v0, v1);
+#pragma unroll
+      for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
+      const uint32_t none = __vcmpeq4(cm, 0u);
+      const uint32_t enew = (__vmaxu4(cm, __vsubus4(eref, 0x5A5A5A5Au)) & ~none) | (eref & none);
+#pragma unroll
+      for (int G4 = 0; G4 < 4; ++G4) {
+        const float f = pow2_diff((eref >> (8 * G4)) & 0xFFu, (int)((enew >> (8 * G4)) & 0xFFu));
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) o[rb][2 * G4 + jj][k4] *= f;
+      }
+      eref = enew;
+      pv_bf16<RB>(o, p, vbase, eref, g);
     } else {
     uint32_t ph[RB][4][2], pl[RB][4][2];
     bool need_lo[4];

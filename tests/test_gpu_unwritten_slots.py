@@ -33,6 +33,7 @@ _EXT = W.CONFIGS["extend_b4_ctx32k_t512"]
 CASES = {
     "decode": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 0),
     "decode_general": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 4),
+    "decode_tcgen05": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 5),
     "verify": (W.scaled(W.CONFIGS["verify_agentic"], batch=4, ctx=("uniform", 300, 1500)), 0),
     "mla": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=("uniform", 17, 900)), 0),
     "extend_tcgen05": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 100, 700)), q_per_seq=40), 0),
