@@ -259,6 +259,8 @@ kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
 #define KV4_KERNEL_GENERAL 4   /* CUDA-core kernel: every shape within the documented row limits */
 #define KV4_KERNEL_TCGEN05 5   /* warp-specialised tcgen05 decode kernel: head_dim 128, <= 8 rows
                                   (T * num_q_heads / num_kv_heads <= 8) */
+#define KV4_KERNEL_LATENT_TC 6 /* warp-specialised tcgen05 latent (MLA) kernel: head_dim 512,
+                                  K = V, <= 16 rows; one CTA per SM */
 
 /* Test controls (bits of diag_flags; 0 in normal use).
  * KV4_DIAG_EXPIRE_FIRST_WAIT: the first bounded wait of every warp that streams

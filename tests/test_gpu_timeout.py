@@ -30,6 +30,7 @@ CASES = {
     "warp_t3": (W.scaled(W.CONFIGS["verify_agentic"], batch=3, ctx=("uniform", 300, 900)), 1),
     "tcgen05": (W.scaled(W.CONFIGS["b32_ctx8k"], batch=3, ctx=("uniform", 100, 900)), 5),
     "latent": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=2, ctx=("uniform", 200, 700)), 3),
+    "latent_tc": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=2, ctx=("uniform", 200, 700)), 6),
     "extend_tc": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 200, 700)), q_per_seq=40), 2),
     "extend_warp": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 200, 700)), q_per_seq=40), 1),
 }

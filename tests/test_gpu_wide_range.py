@@ -37,7 +37,8 @@ CASES = {
     "warp_t3": (W.scaled(_VER, batch=3, ctx=("uniform", 300, 1500)), 0),
     "general": (W.scaled(_B32, batch=2, ctx=("uniform", 200, 900)), 4),
     "tcgen05": (W.scaled(_B32, batch=3, ctx=("uniform", 200, 1500)), 5),
-    "latent": (W.scaled(_MLA, batch=2, ctx=("uniform", 300, 1200)), 0),
+    "latent": (W.scaled(_MLA, batch=2, ctx=("uniform", 300, 1200)), 3),
+    "latent_tc": (W.scaled(_MLA, batch=2, ctx=("uniform", 300, 1200)), 6),
     "extend_tc": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 300, 1100)), q_per_seq=6), 2),
     "extend_warp": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 300, 1100)), q_per_seq=6), 1),
 }
