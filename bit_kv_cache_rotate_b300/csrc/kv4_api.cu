@@ -199,8 +199,8 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
 
   // Kernel choice.  By shape: extend steps (more query rows than the warp-MMA
   // kernel holds per CTA) on the tcgen05 extend kernel, the latent cache on the
-  // latent kernel, head_dim 128 with up to 8 query heads per kv head on the
-  // warp-MMA kernel, everything else on the general kernel.  An explicit
+  // tcgen05 latent kernel, head_dim 128 with up to 8 query heads per kv head on
+  // the warp-MMA kernel, everything else on the general kernel.  An explicit
   // choice (kv4_decode_attention_select) must serve the shape.
   const bool ok_tc = !fp8 && kv4::tc_path_supported(D, G, T, latent);
   const bool ok_ext = !fp8 && kv4::extend_tc_supported(D, G, T, latent);
@@ -216,7 +216,7 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   int k = kernel;
   if (k == KV4_KERNEL_AUTO)
     k = (ok_ext && T * G > 4 * kv4::kTileRows) ? KV4_KERNEL_EXTEND
-        : ok_mla                               ? KV4_KERNEL_LATENT
+        : ok_mla_tc                            ? KV4_KERNEL_LATENT_TC
         : ok_warp                              ? KV4_KERNEL_WARP_MMA
                                                : KV4_KERNEL_GENERAL;
   cudaError_t e;

@@ -34,15 +34,14 @@ struct DecodeArgs {
 // 4-bit kernel's four resident CTAs; measured best at batch 32, 32K context,
 // where more splits add partial-output traffic and per-CTA set-up), at least
 // four pages per split.
-// The latent (head_dim 512) kernel is compute-bound at two CTAs per SM:
-// about one wave, so the split partials stay small.
+// The latent (head_dim 512) tcgen05 kernel holds a whole SM: one wave of at
+// most one CTA per SM (measured best at batch 8, 96K context).
 // Query rows per CTA above which the positions are tiled over CTAs (the
 // warp-MMA kernel's three 8-row blocks).
 constexpr int kTileRows = 24;
 
 inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
-  const int target = head_dim == 512 ? 2 * sms : 7 * sms;
-  int s = (target + units / 2) / units;
+  int s = head_dim == 512 ? sms / units : (7 * sms + units / 2) / units;
   const int cap = max_pages / 4 > 0 ? max_pages / 4 : 1;
   if (s > cap) s = cap;
   if (s > 256) s = 256;

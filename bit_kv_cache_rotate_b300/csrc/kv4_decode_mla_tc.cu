@@ -80,7 +80,8 @@ constexpr int kCvWarps = 4;
 constexpr int kCopyWarp = 8;
 constexpr int kMmaWarp = 9;                        // Q.K^T issue
 constexpr int kPvWarp = 10;                        // P.V issue
-constexpr int kThreads = 11 * 32;
+constexpr int kStatWarp = 11;                      // chunk scale statistics
+constexpr int kThreads = 12 * 32;
 
 // ---- shared memory (bytes)
 // stage: codes [8 pages][4096] (the Q.K^T A operand: token octet o at
@@ -104,16 +105,20 @@ constexpr int kPLbo = (kRows / 8) * 128;                         // 256
 constexpr int kPHalf = (kChunk / 8) * kPLbo;                     // 4096
 constexpr int kPBuf = 2 * kPHalf;                                // 8192
 constexpr int kOffP = kOffVp + 2 * kVpBytes;                     // 202752
+// V factors of a chunk, 2^(e - E_g) as f16 (bf16 when wide) bits:
+// [2 chunks][128 tokens][16 groups]
+constexpr int kFacBytes = kChunk * kGroups * 2;                  // 4096
+constexpr int kOffFac = kOffP + 2 * kPBuf;
 // chunk references: [4 chunks][4 words of group exponents E, flags (bit 0:
 // wide), 3 spare]
 constexpr int kRefRing = 4;
-constexpr int kOffRef = kOffP + 2 * kPBuf;
+constexpr int kOffRef = kOffFac + 2 * kFacBytes;
 // softmax warps' exchange words: [4 warps][16] group bytes and masks, [4
 // warps][16] row maxima or sums, [3 chunks][16] the rows' softmax factors
 constexpr int kXchWords = 2 * kSmWarps * 16 + 3 * kRows;
 constexpr int kOffXch = kOffRef + kRefRing * 8 * 4;
 constexpr int kOffBar = kOffXch + kXchWords * 4;
-constexpr int kNumBars = 34;
+constexpr int kNumBars = 38;
 constexpr int kOffAbort = kOffBar + 8 * kNumBars;
 constexpr int kSmem = kOffAbort + 16;
 // the q-term scale bytes of the prologue [8 terms][16 rows][16 blocks] sit in
@@ -147,6 +152,7 @@ constexpr int kBarPv = 22;         // [3] P.V of a chunk done (commit)
 constexpr int kBarOEmpty = 25;     // [3] O^T of a chunk loaded (4)
 constexpr int kBarCvDone = 28;     // [4] converter warps done with a chunk (4)
 constexpr int kBarDrain = 32;      // [2] every MMA a warp issued done (after a timeout)
+constexpr int kBarRefStats = 34;   // [4] a chunk's group references and wide flag written (1)
 
 // No swizzle: core matrices of 8 x 16 B; lbo = next core matrix along K, sbo
 // = next core matrix along M (N); descriptor version 1.  K-major: a core
@@ -267,6 +273,51 @@ __device__ __forceinline__ uint32_t bf16_pow2(int k) {
   return k >= -126 ? (uint32_t)(127 + k) << 7 : (k >= -133 ? 1u << (k + 133) : 0u);
 }
 
+// One V' tile (tokens 32 j .. 32 j + 31 of the chunk) of converter warp wc.
+// Lane l: token 8 o + l % 8 of each token octet o of the tile, 8-channel block
+// x = l / 8 of each of the warp's groups 4 wc .. 4 wc + 3: four bytes of codes
+// widen to f16, times the token's factor (bf16 for a wide chunk), one 16-byte
+// row of V' (the eight lanes of a store phase write one core matrix).
+template <bool kWide>
+__device__ __forceinline__ void convert_tile(const uint8_t* codes, const uint16_t* fac, uint8_t* vp, int j, int wc,
+                                             int lane) {
+  // every load of the tile first (the stores below may not be moved above
+  // them), then the conversions and the stores
+  uint32_t cw[kSub / 8][4];
+  uint2 f4[kSub / 8];
+#pragma unroll
+  for (int ol = 0; ol < kSub / 8; ++ol) {
+    const int t = 8 * (kSub / 8 * j + ol) + (lane & 7);  // token of the chunk
+    f4[ol] = *reinterpret_cast<const uint2*>(fac + t * kGroups + 4 * wc);
+    const uint8_t* cb =
+        codes + (t >> 4) * kCodeBytes + ((t >> 3) & 1) * 2048 + (4 * wc) * 128 + (t & 7) * 16 + 4 * (lane >> 3);
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) cw[ol][gi] = *reinterpret_cast<const uint32_t*>(cb + gi * 128);
+  }
+#pragma unroll
+  for (int ol = 0; ol < kSub / 8; ++ol) {
+    uint8_t* db = vp + ol * kVpLbo + (16 * wc + (lane >> 3)) * 128 + (lane & 7) * 16;
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      const uint32_t f = __byte_perm(gi < 2 ? f4[ol].x : f4[ol].y, 0u, (gi & 1) ? 0x3232 : 0x1010);
+      const uint32_t w = cw[ol][gi];
+      uint4 out;
+      if (!kWide) {
+        out.x = hmul2(e2m1x2_to_f16x2(w, 0), f);
+        out.y = hmul2(e2m1x2_to_f16x2(w, 1), f);
+        out.z = hmul2(e2m1x2_to_f16x2(w, 2), f);
+        out.w = hmul2(e2m1x2_to_f16x2(w, 3), f);
+      } else {
+        out.x = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(w, 0)), f);
+        out.y = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(w, 1)), f);
+        out.z = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(w, 2)), f);
+        out.w = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(w, 3)), f);
+      }
+      *reinterpret_cast<uint4*>(db + gi * 4 * 128) = out;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -328,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     for (int i = 0; i < kRefRing; ++i) {
       mbar_init(&bars[kBarRefReady + i], kSmWarps);
       mbar_init(&bars[kBarCvDone + i], kCvWarps);
+      mbar_init(&bars[kBarRefStats + i], 1);
     }
     *abort_flag = 0;
   }
@@ -546,6 +598,57 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       }
     }
     if (!ok && lane == 0) *abort_flag = 1;
+  } else if (w == kStatWarp) {
+    // ================================================================ statistics
+    // Chunk c's group references E (each group's largest visible exponent)
+    // and its wide flag (a visible nonzero exponent more than 23 binades below
+    // its group's maximum) into reference slot c % 4, once slot c % 4's last
+    // reader, the fold of chunk c - 4, is done.  Lane l: tokens 4l .. 4l + 3.
+    bool ok = true;
+    for (int c = 0; c < n_chunks && ok; ++c) {
+      const int st = c % kStages, rx = c % kRefRing;
+      ok = wait_or_abort(&bars[kBarFull + st], (uint32_t)((c / kStages) & 1), abort_flag,
+                         c == 0 ? first_limit : kSpinLimit) &&
+           (c < kRefRing ||
+            wait_or_abort(&bars[kBarOEmpty + (c - kRefRing) % kOBufs], (uint32_t)(((c - kRefRing) / kOBufs) & 1),
+                          abort_flag));
+      if (!ok) break;
+      const int pg = p0 + c * kChunkPages;
+      uint32_t mx[4] = {0u, 0u, 0u, 0u}, mn[4] = {~0u, ~0u, ~0u, ~0u};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = 4 * lane + i, pi = t >> 4, tk = t & 15;
+        if (pg + pi < p1 && (pg + pi) * kPage + tk < L) {
+          const uint4 sw = *reinterpret_cast<const uint4*>(smem + kOffStage + st * kStageBytes + kStageCodes +
+                                                           pi * kScaleBytes + tk * 16);
+          const uint32_t sws[4] = {sw.x, sw.y, sw.z, sw.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            mx[q] = __vmaxu4(mx[q], sws[q]);
+            mn[q] = __vminu4(mn[q], sws[q] | __vcmpeq4(sws[q], 0u));
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int o2 = 16; o2 >= 1; o2 >>= 1) {
+          mx[q] = __vmaxu4(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], o2));
+          mn[q] = __vminu4(mn[q], __shfl_xor_sync(0xffffffffu, mn[q], o2));
+        }
+      if (lane == 0) {
+        uint32_t wd = 0u;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ref_s[rx * 8 + q] = mx[q];
+          wd |= __vcmpgtu4(__vsubus4(mx[q], mn[q]), 0x17171717u);
+        }
+        ref_s[rx * 8 + 4] = wd != 0u ? 1u : 0u;
+        mbar_arrive(&bars[kBarRefStats + rx]);
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
   } else if (w >= kSmWarps) {
     // ================================================================ converters
     const int wc = w - kSmWarps;
@@ -556,12 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
                          c == 0 ? first_limit : kSpinLimit) &&
            wait_or_abort(&bars[kBarRefReady + rx], (uint32_t)((c / kRefRing) & 1), abort_flag);
       if (!ok) break;
-      const uint32_t* ref = ref_s + rx * 8;
-      const uint32_t E4[4] = {ref[0], ref[1], ref[2], ref[3]};
-      const bool wide = (ref[4] & 1u) != 0u;
+      const bool wide = (ref_s[rx * 8 + 4] & 1u) != 0u;
       const uint8_t* codes = smem + kOffStage + st * kStageBytes;
-      const uint8_t* scales = codes + kStageCodes;
-      const int pg = p0 + c * kChunkPages;
+      const uint16_t* fac = reinterpret_cast<const uint16_t*>(smem + kOffFac + (c & 1) * kFacBytes);
       for (int j = 0; j < kSubs && ok; ++j) {
         const int gj = kSubs * c + j, vb = gj & 1;
         if (gj >= 2) {
@@ -569,38 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
           if (!ok) break;
         }
         uint8_t* vp = smem + kOffVp + vb * kVpBytes;
-        // tasks: token octet ol of the tile x channel group 4 wc + gi.  Lane l
-        // = (token 8 o + l % 8, 8-channel block x = l / 8): four bytes of codes
-        // widen to f16, times the token's factor 2^(e - E_g) (0 for a token
-        // past the split or the context), one 16-byte row of V' (the eight
-        // lanes of a store phase write one 128-byte core matrix).
-#pragma unroll 2
-        for (int task = 0; task < 16; ++task) {
-          const int ol = task >> 2, gi = task & 3, g = 4 * wc + gi;
-          const int o = kSub / 8 * j + ol;          // token octet of the chunk
-          const int t = 8 * o + (lane & 7);         // token of the chunk
-          const int x = lane >> 3;                  // channels 32 g + 8 x .. + 7
-          const uint32_t cw = *reinterpret_cast<const uint32_t*>(codes + (t >> 4) * kCodeBytes +
-                                                                ((t >> 3) & 1) * 2048 + g * 128 + (t & 7) * 16 + 4 * x);
-          const int e = scales[(t >> 4) * kScaleBytes + (t & 15) * 16 + g];
-          const int k = e - (int)((E4[g >> 2] >> (8 * (g & 3))) & 0xFFu);
-          const bool vis = pg + (t >> 4) < p1 && (pg + (t >> 4)) * kPage + (t & 15) < L;
-          const uint32_t f1 = !vis ? 0u : (wide ? bf16_pow2(k) : f16_pow2(k));
-          const uint32_t f = f1 | (f1 << 16);
-          uint4 out;
-          if (!wide) {
-            out.x = hmul2(e2m1x2_to_f16x2(cw, 0), f);
-            out.y = hmul2(e2m1x2_to_f16x2(cw, 1), f);
-            out.z = hmul2(e2m1x2_to_f16x2(cw, 2), f);
-            out.w = hmul2(e2m1x2_to_f16x2(cw, 3), f);
-          } else {
-            out.x = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(cw, 0)), f);
-            out.y = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(cw, 1)), f);
-            out.z = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(cw, 2)), f);
-            out.w = bmul2(f16x2_to_bf16x2(e2m1x2_to_f16x2(cw, 3)), f);
-          }
-          *reinterpret_cast<uint4*>(vp + ol * kVpLbo + (4 * g + x) * 128 + (t & 7) * 16) = out;
-        }
+        if (!wide)
+          convert_tile<false>(codes, fac, vp, j, wc, lane);
+        else
+          convert_tile<true>(codes, fac, vp, j, wc, lane);
         fence_proxy_async();  // V' written by ordinary stores, read by the MMA
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kBarVpFull + vb]);
@@ -655,62 +727,56 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       return true;
     };
 
-    // Chunk x's group references E (each group's largest visible exponent)
-    // and its wide flag, into reference slot x % 4 (the stage still holds the
-    // chunk: its logits are not loaded yet); the converters compute their V
-    // factors 2^(e - E_g) from them.  `good` carries an earlier failure of
-    // this warp into the barrier, where the four warps agree; false (for all
-    // four) when any of them failed.
+    // This token's V factors of chunk x, 2^(e - E_g) as f16 bits (bf16 when
+    // the chunk is wide; 0 if the token is invisible), from the chunk's
+    // references (statistics warp) into factor buffer x % 2, once the
+    // converters are done with chunk x - 2.  Per warp; false when a wait
+    // failed.
     auto publish_ref = [&](int x, bool good) -> bool {
       const int st = x % kStages, rx = x % kRefRing;
-      // the converters are done with slot x % 4 (chunk x - 4)
-      if (good && x >= kRefRing)
-        good = wait_or_abort(&bars[kBarCvDone + rx], (uint32_t)(((x - kRefRing) / kRefRing) & 1), abort_flag);
-      if (!good && lane == 0) *abort_flag = 1;
+      if (good)
+        good = wait_or_abort(&bars[kBarRefStats + rx], (uint32_t)((x / kRefRing) & 1), abort_flag);
+      if (good && x >= 2)
+        good = wait_or_abort(&bars[kBarCvDone + (x - 2) % kRefRing], (uint32_t)(((x - 2) / kRefRing) & 1), abort_flag);
+      if (!good) {
+        if (lane == 0) *abort_flag = 1;
+        return false;
+      }
       const int pg = p0 + x * kChunkPages;
       const int pi = m >> 4, tk = m & 15;
-      const bool vis = good && pg + pi < p1 && (pg + pi) * kPage + tk < L;
-      uint4 sw = make_uint4(0u, 0u, 0u, 0u);
-      if (vis)
-        sw = *reinterpret_cast<const uint4*>(smem + kOffStage + st * kStageBytes + kStageCodes + pi * kScaleBytes +
-                                             tk * 16);
-      const uint32_t sws[4] = {sw.x, sw.y, sw.z, sw.w};
-      // group maxima (E) and smallest nonzero exponents over the visible tokens
-      uint32_t mx[4], mn[4];
+      const bool vis = pg + pi < p1 && (pg + pi) * kPage + tk < L;
+      uint32_t fw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      if (vis) {
+        const uint4 sw = *reinterpret_cast<const uint4*>(smem + kOffStage + st * kStageBytes + kStageCodes +
+                                                         pi * kScaleBytes + tk * 16);
+        const uint32_t sws[4] = {sw.x, sw.y, sw.z, sw.w};
+        const bool wd = (ref_s[rx * 8 + 4] & 1u) != 0u;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mx[i] = sws[i];
-        mn[i] = vis ? (sws[i] | __vcmpeq4(sws[i], 0u)) : 0xFFFFFFFFu;
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t Eq = ref_s[rx * 8 + q];
+          const uint32_t d = __vsubus4(Eq, sws[q]);  // E_g - e >= 0 per group
+          // exponent field of 2^-d: 15 - d (f16) or 127 - d (bf16), four groups
+          // at once; a factor below the normal range (d > 14 f16, d > 126
+          // bf16: rare) takes the scalar form
+          const uint32_t top = wd ? 0x7E7E7E7Eu : 0x0E0E0E0Eu;
+          if (__vcmpgtu4(d, top) == 0u) {
+            const uint32_t fld = __vsubus4(wd ? 0x7F7F7F7Fu : 0x0F0F0F0Fu, d);
+            const int sh = wd ? 7 : 10;
+            fw[2 * q] = __byte_perm(fld, 0u, 0x5140) << sh;      // groups 4q, 4q + 1
+            fw[2 * q + 1] = __byte_perm(fld, 0u, 0x5342) << sh;  // groups 4q + 2, 4q + 3
+          } else {
 #pragma unroll
-        for (int o2 = 16; o2 >= 1; o2 >>= 1) {
-          mx[i] = __vmaxu4(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], o2));
-          mn[i] = __vminu4(mn[i], __shfl_xor_sync(0xffffffffu, mn[i], o2));
-        }
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          xchu[w * 16 + i] = mx[i];
-          xchu[w * 16 + 4 + i] = mn[i];
-        }
-      }
-      if (bar_or(1, kSmWarps * 32, !good)) return false;
-      if (tid == 0) {
-        uint32_t wd = 0u;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t M = xchu[i], N = xchu[4 + i];
-#pragma unroll
-          for (int ww = 1; ww < kSmWarps; ++ww) {
-            M = __vmaxu4(M, xchu[ww * 16 + i]);
-            N = __vminu4(N, xchu[ww * 16 + 4 + i]);
+            for (int u = 0; u < 4; ++u) {
+              const int k = -(int)((d >> (8 * u)) & 0xFFu);
+              const uint32_t bits = wd ? bf16_pow2(k) : f16_pow2(k);
+              fw[2 * q + (u >> 1)] |= bits << (16 * (u & 1));
+            }
           }
-          ref_s[rx * 8 + i] = M;
-          // a visible exponent more than 23 binades below its group's maximum
-          wd |= __vcmpgtu4(__vsubus4(M, N), 0x17171717u);
         }
-        ref_s[rx * 8 + 4] = wd != 0u ? 1u : 0u;
       }
+      uint4* fd = reinterpret_cast<uint4*>(smem + kOffFac + (x & 1) * kFacBytes + m * kGroups * 2);
+      fd[0] = make_uint4(fw[0], fw[1], fw[2], fw[3]);
+      fd[1] = make_uint4(fw[4], fw[5], fw[6], fw[7]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarRefReady + rx]);
       return true;
@@ -771,6 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     // where all four warps take part, turns it into a common exit.
     ok = place_sfa(0, true);
     ok = publish_ref(0, ok);
+    ok = !bar_or(1, kSmWarps * 32, !ok);
     bool good = true;
     for (int c = 0; c < n_chunks && ok; ++c) {
       const int st = c % kStages, bb = c & 1;
@@ -885,11 +952,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       fence_proxy_async();
       __syncwarp();
       if (good && lane == 0) mbar_arrive(&bars[kBarP + bb]);
-      // ---- references of chunk c + 1 (the converters start on it)
-      if (c + 1 < n_chunks && !publish_ref(c + 1, good)) {
-        ok = false;
-        break;
-      }
+      // ---- V factors of chunk c + 1 (the converters start on it)
+      if (c + 1 < n_chunks) good = publish_ref(c + 1, good);
       // ---- fold chunk c - 2 (its P.V finished before P^T of chunk c went in)
       if (good && c >= 2) good = fold(c - 2);
       if (!good && lane == 0) *abort_flag = 1;

@@ -255,7 +255,7 @@ kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
 #define KV4_KERNEL_WARP_MMA 1  /* warp-MMA kernel: head_dim 128, <= 8 query heads per kv head;
                                   up to 24 rows per CTA, more rows as position tiles */
 #define KV4_KERNEL_EXTEND 2    /* tcgen05 extend kernel: head_dim 128, G in {1,2,4,8}, > 24 rows */
-#define KV4_KERNEL_LATENT 3    /* latent (MLA) kernel: head_dim 512, K = V, <= 16 rows */
+#define KV4_KERNEL_LATENT 3    /* warp-MMA latent (MLA) kernel: head_dim 512, K = V, <= 16 rows */
 #define KV4_KERNEL_GENERAL 4   /* CUDA-core kernel: every shape within the documented row limits */
 #define KV4_KERNEL_TCGEN05 5   /* warp-specialised tcgen05 decode kernel: head_dim 128, <= 8 rows
                                   (T * num_q_heads / num_kv_heads <= 8) */

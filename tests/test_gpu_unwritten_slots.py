@@ -36,6 +36,7 @@ CASES = {
     "decode_tcgen05": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 5),
     "verify": (W.scaled(W.CONFIGS["verify_agentic"], batch=4, ctx=("uniform", 300, 1500)), 0),
     "mla": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=("uniform", 17, 900)), 0),
+    "mla_warp": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=("uniform", 17, 900)), 3),
     "extend_tcgen05": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 100, 700)), q_per_seq=40), 0),
     "extend_warp": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 100, 700)), q_per_seq=40), 1),
     "general_g10": (dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), num_q_heads=80), 0),
