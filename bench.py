@@ -268,6 +268,15 @@ def run_ours(args, rank, world, local_rank):
         kv4.kv4_append_quantize(wl.new_k, wl.new_v, wl.new_slots, wl.kc, wl.vc, lay.num_pages)
         if ev_a is not None:
             ev_a.record(cur)
+        if args.kernel:
+            # an explicit split kernel: split + combine in one call (the events
+            # then bracket both; the combine is a few microseconds)
+            kv4.kv4_decode_attention_select(wl.q, wl.kc, wl.vc, wl.tab, wl.lens, cfg.num_kv_heads, lay.num_pages,
+                                            cfg.softmax_scale, args.kernel, num_splits=wl.S, workspace_buf=wl.ws,
+                                            out=wl.out)
+            if ev_b is not None:
+                ev_b.record(cur)
+            return
         kv4.kv4_decode_partials(wl.q, wl.kc, wl.vc, wl.tab, wl.lens, cfg.num_kv_heads, lay.num_pages,
                                 cfg.softmax_scale, wl.S, wl.ws)
         if ev_b is not None:
@@ -457,9 +466,11 @@ def run_ours(args, rank, world, local_rank):
         achieved = nbytes / (kern_ms * 1e-3) / 1e9
         metric, unit = METRIC, "GB/s"
         e2e_value = replica_gbs(nbytes, world, e2e_ms)
-        roofline = {"bound": "hbm", "kernel": "kv4 decode split kernel", "achieved": round(achieved, 1),
+        roofline = {"bound": "hbm", "kernel": "kv4 decode split kernel" + (f" (kernel {args.kernel}, with the combine)"
+                                                                        if args.kernel else ""),
+                    "achieved": round(achieved, 1),
                     "peak": peak, "peak_kind": f"{peak_kind} (hbm copy)", "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": stored_traffic(cfg.name),
+                    "frac": round(achieved / peak, 4), "traffic": (stored_traffic(cfg.name) if not args.kernel else None),
                     "kernel_ms": round(kern_ms, 5)}
     res = {
         "metric": metric,
@@ -614,6 +625,8 @@ def main():
     ap.add_argument("--config", default="b32_ctx32k", choices=sorted(W.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="explicit split kernel (KV4_KERNEL_*); 0 = the automatic choice")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

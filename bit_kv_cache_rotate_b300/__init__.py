@@ -29,7 +29,7 @@ KV4_OK, KV4_ERR_INVALID_ARG, KV4_ERR_UNSUPPORTED, KV4_ERR_CUDA, KV4_ERR_DEVICE_B
 KV4_DEVERR_PAGE, KV4_DEVERR_CONTEXT, KV4_DEVERR_SLOT, KV4_DEVERR_TIMEOUT = 1, 2, 4, 8
 # kernel choices and test controls of kv4_decode_attention_select (include/kv4.h)
 (KV4_KERNEL_AUTO, KV4_KERNEL_WARP_MMA, KV4_KERNEL_EXTEND, KV4_KERNEL_LATENT, KV4_KERNEL_GENERAL,
- KV4_KERNEL_TCGEN05, KV4_KERNEL_LATENT_TC) = range(7)
+ KV4_KERNEL_TCGEN05, KV4_KERNEL_LATENT_TC, KV4_KERNEL_BALANCED) = range(8)
 KV4_DIAG_EXPIRE_FIRST_WAIT = 1
 KV4_MAX_Q_PER_SEQ = 4096  # include/kv4.h
 PAGE_SIZE = 16

@@ -206,6 +206,7 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   const bool ok_ext = !fp8 && kv4::extend_tc_supported(D, G, T, latent);
   const bool ok_mla = !fp8 && kv4::mla_path_supported(D, G, T, latent);
   const bool ok_mla_tc = !fp8 && kv4::mla_tc_path_supported(D, G, T, latent);
+  const bool ok_flat = !fp8 && causal && kv4::flat_path_supported(D, G, T, latent, S);
   const bool ok_warp = fp8 ? kv4::fp8_fast_path_supported(D, G, T) : kv4::fast_path_supported(D, G, T, latent);
   const bool ok_gen = T * G <= kv4::ref_max_rows(D);
   // The extend kernel's tile is 128 query rows; a block of a few positions
@@ -236,6 +237,10 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
     case KV4_KERNEL_LATENT_TC:
       if (!ok_mla_tc) return KV4_ERR_UNSUPPORTED;
       e = kv4::launch_decode_mla_tc(a, st);
+      break;
+    case KV4_KERNEL_BALANCED:
+      if (!ok_flat) return KV4_ERR_UNSUPPORTED;
+      e = kv4::launch_decode_flat(a, st);
       break;
     case KV4_KERNEL_WARP_MMA:
       if (!ok_warp) return KV4_ERR_UNSUPPORTED;

@@ -54,6 +54,8 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st);
 bool mla_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st);
 bool mla_tc_path_supported(int D, int G, int T, bool latent);
+bool flat_path_supported(int D, int G, int T, bool latent, int S);
+cudaError_t launch_decode_flat(const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, cudaStream_t st);
 bool tc_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);

@@ -261,6 +261,8 @@ kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
                                   (T * num_q_heads / num_kv_heads <= 8) */
 #define KV4_KERNEL_LATENT_TC 6 /* warp-specialised tcgen05 latent (MLA) kernel: head_dim 512,
                                   K = V, <= 16 rows; one CTA per SM */
+#define KV4_KERNEL_BALANCED 7  /* balanced warp-MMA kernel: head_dim 128, <= 8 rows, num_splits >= 2,
+                                  not the prefix form; one CTA per SM, chunks shared by its warps */
 
 /* Test controls (bits of diag_flags; 0 in normal use).
  * KV4_DIAG_EXPIRE_FIRST_WAIT: the first bounded wait of every warp that streams

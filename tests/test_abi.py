@@ -168,7 +168,7 @@ def test_kernel_choice_is_validated_before_launch(lib):
     assert sel(*args(-1)) == kv4.KV4_ERR_INVALID_ARG
     assert sel(*args(kv4.KV4_KERNEL_LATENT)) == kv4.KV4_ERR_UNSUPPORTED        # not a latent cache
     assert sel(*args(kv4.KV4_KERNEL_LATENT_TC)) == kv4.KV4_ERR_UNSUPPORTED     # not a latent cache
-    assert sel(*args(7)) == kv4.KV4_ERR_INVALID_ARG
+    assert sel(*args(8)) == kv4.KV4_ERR_INVALID_ARG
     assert sel(*args(kv4.KV4_KERNEL_EXTEND)) == kv4.KV4_ERR_UNSUPPORTED        # 4 rows: not an extend tile
     assert sel(*args(kv4.KV4_KERNEL_WARP_MMA, D=64)) == kv4.KV4_ERR_UNSUPPORTED  # head_dim 64
     assert sel(*args(kv4.KV4_KERNEL_GENERAL, T=40, Hq=16)) == kv4.KV4_ERR_UNSUPPORTED  # 320 rows

@@ -29,6 +29,7 @@ CASES = {
     "warp_t1": (W.scaled(W.CONFIGS["b32_ctx8k"], batch=3, ctx=("uniform", 100, 900)), 1),
     "warp_t3": (W.scaled(W.CONFIGS["verify_agentic"], batch=3, ctx=("uniform", 300, 900)), 1),
     "tcgen05": (W.scaled(W.CONFIGS["b32_ctx8k"], batch=3, ctx=("uniform", 100, 900)), 5),
+    "balanced": (W.scaled(W.CONFIGS["b32_ctx8k"], batch=3, ctx=("uniform", 100, 900)), 7),
     "latent": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=2, ctx=("uniform", 200, 700)), 3),
     "latent_tc": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=2, ctx=("uniform", 200, 700)), 6),
     "extend_tc": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 200, 700)), q_per_seq=40), 2),
@@ -46,7 +47,7 @@ def test_expired_wait_flags_timeout_and_the_next_call_is_correct(name):
     q = W.queries(cfg)
     tab, lens = gpu_tables(lay)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for S in (1, 2):
+    for S in ((2, 3) if kernel == kv4.KV4_KERNEL_BALANCED else (1, 2)):
         err.zero_()
         kv4.kv4_decode_attention_select(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
                                         cfg.softmax_scale, kernel, diag_flags=kv4.KV4_DIAG_EXPIRE_FIRST_WAIT,

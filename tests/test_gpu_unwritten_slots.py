@@ -34,6 +34,7 @@ CASES = {
     "decode": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 0),
     "decode_general": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 4),
     "decode_tcgen05": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 5),
+    "decode_balanced": (W.scaled(_B32, batch=3, ctx=("uniform", 17, 700)), 7),
     "verify": (W.scaled(W.CONFIGS["verify_agentic"], batch=4, ctx=("uniform", 300, 1500)), 0),
     "mla": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=("uniform", 17, 900)), 0),
     "mla_warp": (W.scaled(W.CONFIGS["mla_b8_ctx96k"], batch=3, ctx=("uniform", 17, 900)), 3),
@@ -56,7 +57,7 @@ def test_4bit_attention_ignores_unwritten_slots(name, fill):
     q = W.queries(cfg)
     tab, lens = gpu_tables(lay)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for S in (1, 3):
+    for S in ((2, 3) if kernel == kv4.KV4_KERNEL_BALANCED else (1, 3)):
         out = kv4.kv4_decode_attention_select(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
                                               cfg.softmax_scale, kernel, num_splits=S, dev_error=err)
         torch.cuda.synchronize()

@@ -37,6 +37,7 @@ CASES = {
     "warp_t3": (W.scaled(_VER, batch=3, ctx=("uniform", 300, 1500)), 0),
     "general": (W.scaled(_B32, batch=2, ctx=("uniform", 200, 900)), 4),
     "tcgen05": (W.scaled(_B32, batch=3, ctx=("uniform", 200, 1500)), 5),
+    "balanced": (W.scaled(_B32, batch=3, ctx=("uniform", 200, 1500)), 7),
     "latent": (W.scaled(_MLA, batch=2, ctx=("uniform", 300, 1200)), 3),
     "latent_tc": (W.scaled(_MLA, batch=2, ctx=("uniform", 300, 1200)), 6),
     "extend_tc": (dataclasses.replace(W.scaled(_EXT, batch=2, ctx=("uniform", 300, 1100)), q_per_seq=6), 2),
@@ -95,7 +96,7 @@ def test_wide_v_scale_range(name, log2_scale):
     assert np.abs(ref).max() < 100.0
     tab, lens = gpu_tables(lay)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for S in (1, 3):
+    for S in ((2, 3) if kernel == kv4.KV4_KERNEL_BALANCED else (1, 3)):
         out = kv4.kv4_decode_attention_select(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
                                               cfg.softmax_scale, kernel, num_splits=S, dev_error=err)
         torch.cuda.synchronize()
