@@ -46,8 +46,12 @@ FALLBACK_BF16_TFLOPS = 1800.0
 DECODE_SOURCES = ("bit_kv_cache_rotate_b300/csrc/kv4_decode_mma.cu",
                   "bit_kv_cache_rotate_b300/csrc/kv4_extend_tc.cu",
                   "bit_kv_cache_rotate_b300/csrc/kv4_decode_mla.cu",
+                  "bit_kv_cache_rotate_b300/csrc/kv4_decode_mla_tc.cu",
                   "bit_kv_cache_rotate_b300/csrc/kv4_mma_common.cuh",
                   "bit_kv_cache_rotate_b300/csrc/kv4_decode.h")
+KERNEL_NAMES = {1: "warp-MMA kernel, split form", 2: "tcgen05 extend kernel", 3: "warp-MMA latent kernel",
+                4: "general CUDA-core kernel", 5: "warp-specialised tcgen05 decode kernel",
+                6: "tcgen05 latent kernel", 7: "warp-MMA kernel, flat mode"}
 METRIC = "4-bit-KV decode attention: HBM GB/s (% of peak) and ms/step at 32K ctx, batch 32"
 EXTEND_METRIC = "4-bit-KV extend attention: TFLOP/s (% of peak) and ms/step"
 
@@ -466,8 +470,10 @@ def run_ours(args, rank, world, local_rank):
         achieved = nbytes / (kern_ms * 1e-3) / 1e9
         metric, unit = METRIC, "GB/s"
         e2e_value = replica_gbs(nbytes, world, e2e_ms)
-        roofline = {"bound": "hbm", "kernel": "kv4 decode split kernel" + (f" (kernel {args.kernel}, with the combine)"
-                                                                        if args.kernel else ""),
+        kid = args.kernel or kv4.kv4_decode_kernel_choice(cfg.batch, cfg.q_per_seq, cfg.num_q_heads,
+                                                          cfg.num_kv_heads, cfg.head_dim, wl.S, cfg.latent)
+        roofline = {"bound": "hbm", "kernel": f"kv4 decode split kernel: {KERNEL_NAMES.get(kid, kid)}"
+                                              + (" (explicit choice, timed with the combine)" if args.kernel else ""),
                     "achieved": round(achieved, 1),
                     "peak": peak, "peak_kind": f"{peak_kind} (hbm copy)", "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": (stored_traffic(cfg.name) if not args.kernel else None),

@@ -37,7 +37,8 @@ PAGE_SIZE = 16
 EXPORTS = ("kv4_status_string", "kv4_cache_bytes", "kv4_append_quantize", "kv4_decode_auto_splits",
            "kv4_decode_workspace_bytes", "kv4_decode_attention", "kv4_decode_partials", "kv4_split_combine",
            "fp8_cache_bytes", "fp8_append_quantize", "fp8_decode_attention",
-           "kv4_decode_attention_noalloc", "kv4_decode_attention_select", "kv4_decode_partials_prefix")
+           "kv4_decode_attention_noalloc", "kv4_decode_attention_select", "kv4_decode_partials_prefix",
+           "kv4_decode_kernel_choice")
 
 
 class Kv4Error(RuntimeError):
@@ -63,6 +64,8 @@ def _load() -> ctypes.CDLL:
     L.fp8_append_quantize.restype = i32
     L.kv4_decode_auto_splits.argtypes = [i32] * 7
     L.kv4_decode_auto_splits.restype = i32
+    L.kv4_decode_kernel_choice.argtypes = [i32] * 7
+    L.kv4_decode_kernel_choice.restype = i32
     L.kv4_decode_workspace_bytes.argtypes = [i32] * 5
     L.kv4_decode_workspace_bytes.restype = sz
     L.kv4_decode_attention.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32,
@@ -131,6 +134,12 @@ def kv4_cache_bytes(num_pages: int, num_kv_heads: int, page_size: int, head_dim:
 
 def fp8_cache_bytes(num_pages: int, num_kv_heads: int, page_size: int, head_dim: int) -> int:
     return int(lib().fp8_cache_bytes(num_pages, num_kv_heads, page_size, head_dim))
+
+
+def kv4_decode_kernel_choice(batch, q_per_seq, num_q_heads, num_kv_heads, head_dim, num_splits, latent=False) -> int:
+    """The KV4_KERNEL_* id kv4_decode_attention runs for this shape (-1: invalid shape)."""
+    return int(lib().kv4_decode_kernel_choice(batch, q_per_seq, num_q_heads, num_kv_heads, head_dim, num_splits,
+                                              1 if latent else 0))
 
 
 def kv4_decode_auto_splits(batch, q_per_seq, num_q_heads, num_kv_heads, head_dim, page_size,

@@ -136,6 +136,39 @@ size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int
   return ((o + 255) / 256) * 256 + l;
 }
 
+// Automatic kernel choice.  By shape: extend steps (more query rows than the
+// warp-MMA kernel holds per CTA) on the tcgen05 extend kernel, the latent
+// cache on the tcgen05 latent kernel, head_dim 128 with up to 24 query rows
+// per kv head on the warp-MMA kernel, everything else on the general kernel.
+// The extend kernel's tile is 128 query rows; a block of a few positions (a
+// 6-token verify: 48 rows) leaves most of it idle and runs slower than the
+// warp-MMA kernel's position tiles reading the pages once per 24 rows (L2
+// serves the repeats), so only blocks above 96 rows (four tiles of 24) go to
+// the extend kernel.  Up to 8 rows per kv head, the warp-MMA kernel runs in
+// flat mode (one wave of CTAs over equal parts of the step's chunks) when the
+// S slots allow a wave's worth of equal parts of sequences of the table's full
+// length: (S - 1) x units >= the wave's CTAs; otherwise (few slots for many
+// sequences) the split form.
+static int auto_kernel(bool fp8, int D, int G, int T, bool latent, bool causal, int S, long long units) {
+  if (!fp8 && kv4::extend_tc_supported(D, G, T, latent) && T * G > 4 * kv4::kTileRows) return KV4_KERNEL_EXTEND;
+  if (!fp8 && kv4::mla_tc_path_supported(D, G, T, latent)) return KV4_KERNEL_LATENT_TC;
+  if (!fp8 && causal && kv4::flat_path_supported(D, G, T, latent, S)) {
+    const int grid = kv4::flat_grid_size();
+    if (grid > 0 && (long long)(S - 1) * units >= grid) return KV4_KERNEL_BALANCED;
+  }
+  const bool ok_warp = fp8 ? kv4::fp8_fast_path_supported(D, G, T) : kv4::fast_path_supported(D, G, T, latent);
+  return ok_warp ? KV4_KERNEL_WARP_MMA : KV4_KERNEL_GENERAL;
+}
+
+int kv4_decode_kernel_choice(int batch, int q_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
+                             int num_splits, int latent) {
+  if (batch < 1 || q_per_seq < 1 || num_kv_heads < 1 || num_q_heads < num_kv_heads || num_q_heads % num_kv_heads ||
+      !valid_dim(head_dim) || num_splits < 1)
+    return -1;
+  return auto_kernel(false, head_dim, num_q_heads / num_kv_heads, q_per_seq, latent != 0, true, num_splits,
+                     (long long)batch * num_kv_heads);
+}
+
 static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
                                 const uint8_t* v_cache, const float* k_scale,
                                 const float* v_scale, const int32_t* block_tables,
@@ -197,11 +230,7 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   a.pos_split = 0;
   a.pos_tile = 1;
 
-  // Kernel choice.  By shape: extend steps (more query rows than the warp-MMA
-  // kernel holds per CTA) on the tcgen05 extend kernel, the latent cache on the
-  // tcgen05 latent kernel, head_dim 128 with up to 8 query heads per kv head on
-  // the warp-MMA kernel, everything else on the general kernel.  An explicit
-  // choice (kv4_decode_attention_select) must serve the shape.
+  // An explicit choice (kv4_decode_attention_select) must serve the shape.
   const bool ok_tc = !fp8 && kv4::tc_path_supported(D, G, T, latent);
   const bool ok_ext = !fp8 && kv4::extend_tc_supported(D, G, T, latent);
   const bool ok_mla = !fp8 && kv4::mla_path_supported(D, G, T, latent);
@@ -209,17 +238,8 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
   const bool ok_flat = !fp8 && causal && kv4::flat_path_supported(D, G, T, latent, S);
   const bool ok_warp = fp8 ? kv4::fp8_fast_path_supported(D, G, T) : kv4::fast_path_supported(D, G, T, latent);
   const bool ok_gen = T * G <= kv4::ref_max_rows(D);
-  // The extend kernel's tile is 128 query rows; a block of a few positions
-  // (a 6-token verify: 48 rows) leaves most of it idle and runs slower than the
-  // warp-MMA kernel's position tiles reading the pages once per 24 rows (L2
-  // serves the repeats), so automatic choice sends only blocks above 96 rows
-  // (four tiles of 24) to the extend kernel.
-  int k = kernel;
-  if (k == KV4_KERNEL_AUTO)
-    k = (ok_ext && T * G > 4 * kv4::kTileRows) ? KV4_KERNEL_EXTEND
-        : ok_mla_tc                            ? KV4_KERNEL_LATENT_TC
-        : ok_warp                              ? KV4_KERNEL_WARP_MMA
-                                               : KV4_KERNEL_GENERAL;
+  const int k = kernel == KV4_KERNEL_AUTO ? auto_kernel(fp8, D, G, T, latent, causal, S, (long long)batch * Hkv)
+                                          : kernel;
   cudaError_t e;
   switch (k) {
     case KV4_KERNEL_TCGEN05:
@@ -240,7 +260,7 @@ static kv4_status decode_common(bool fp8, const void* q, const uint8_t* k_cache,
       break;
     case KV4_KERNEL_BALANCED:
       if (!ok_flat) return KV4_ERR_UNSUPPORTED;
-      e = kv4::launch_decode_flat(a, st);
+      e = kv4::launch_decode_fast(D, a, st, true);
       break;
     case KV4_KERNEL_WARP_MMA:
       if (!ok_warp) return KV4_ERR_UNSUPPORTED;

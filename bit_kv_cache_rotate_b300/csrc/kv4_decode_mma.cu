@@ -150,12 +150,134 @@ __device__ __forceinline__ void pv_bf16(float (&o)[RB][8][4], const float2 (&p)[
 // carry zero q and are never written.  Each K and V fragment is widened once
 // and used by every row block (a T = 3 verify step shares the decode work of
 // its three positions).
-template <int RB>
+template <int RB, bool FLAT>
 __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     decode_fp4_mma_kernel(DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<RB> sm{smem_raw};
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = a.Hq / a.Hkv;
+  uint64_t* bars = sm.bars();  // [kWarps][kStages]
+
+  // ---- barriers, once: a warp's k-th chunk (over all its units) uses stage
+  // k % kStages with phase (k / kStages) & 1
+  if (lane == 0)
+    for (int i = 0; i < kStages; ++i) mbar_init(&bars[w * kStages + i], 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  int it_base = 0;  // this warp's chunks in earlier units
+  const int first_limit = (a.diag & KV4_DIAG_EXPIRE_FIRST_WAIT) ? 0 : kSpinLimit;
+
+  // ---- flat mode: CTA i takes the i-th equal part of the flat range of 4-page
+  // chunks in (sequence, kv head, chunk) order and runs each (sequence, kv
+  // head) run of it as one unit, writing that unit's partial in slot (CTA -
+  // the unit's first CTA).  The part size keeps every (sequence, kv head)
+  // within S CTAs; the CTA holding its last chunk writes the unused slots as
+  // empty partials, so the combine merges them like the split form's.
+  __shared__ long long fl_cur, fl_hi, fl_per;
+  __shared__ int fl_unit[6];  // b, h, first chunk, end chunk, slot, first empty slot
+  __shared__ int fl_stop;
+  auto fl_valid = [&](int Ls) { return Ls >= a.T && Ls <= a.max_pages * kPage; };
+  auto fl_chunks = [&](int Ls) { return ((Ls + kPage - 1) / kPage + kPagesPerChunk - 1) / kPagesPerChunk; };
+  if constexpr (FLAT) {
+    if (w == 0) {
+      long long C = 0;
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int bq = b0 + lane;
+        const int Ls = bq < a.B ? a.context_lens[bq] : 0;
+        const int nc = bq < a.B && fl_valid(Ls) ? fl_chunks(Ls) : 0;
+        C += (long long)__reduce_add_sync(0xffffffffu, (unsigned)nc) * a.Hkv;
+      }
+      if (lane == 0) {
+        const long long nc_max = (a.max_pages + kPagesPerChunk - 1) / kPagesPerChunk;
+        const long long even = (C + gridDim.x - 1) / gridDim.x;
+        const long long bound = (nc_max + a.S - 2) / (a.S - 1);
+        const long long per = even > bound ? even : bound;
+        fl_per = per > 0 ? per : 1;
+        fl_cur = (long long)blockIdx.x * fl_per;
+        fl_hi = fl_cur + fl_per < C ? fl_cur + fl_per : C;
+        fl_stop = 0;
+      }
+    }
+    // CTA 0: sequences whose context is out of range get empty partials
+    if (blockIdx.x == 0) {
+      const int R0 = a.T * G;
+      for (int bq = w; bq < a.B; bq += kWarps) {
+        if (fl_valid(a.context_lens[bq])) continue;
+        if (lane == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
+        for (int hh = 0; hh < a.Hkv; ++hh)
+          for (int r = 0; r < R0; ++r) {
+            const size_t row = ((size_t)bq * a.T + r / G) * a.Hq + hh * G + (r % G);
+            for (int sl = 0; sl < a.S; ++sl) {
+              for (int d = lane; d < D; d += 32) a.part_o[(row * a.S + sl) * D + d] = 0.0f;
+              if (lane == 0) a.part_lse[row * a.S + sl] = -INFINITY;
+            }
+          }
+      }
+    }
+    __syncthreads();
+  }
+
+  for (;;) {  // units: one in the split form, the runs of this CTA's part in flat mode
+  int b, h, s, c_first = 0, c_end = 0, empty_from = 0;
+  if constexpr (FLAT) {
+    if (fl_cur >= fl_hi || fl_stop) break;
+    // the (sequence, kv head) holding chunk fl_cur
+    if (w == 0) {
+      const long long cur = fl_cur, hi = fl_hi, per = fl_per;
+      long long base = 0;
+      bool found = false;
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int bq = b0 + lane;
+        const int Ls = bq < a.B ? a.context_lens[bq] : 0;
+        const int nc = bq < a.B && fl_valid(Ls) ? fl_chunks(Ls) : 0;
+        int incl = nc;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o2);
+          if (lane >= o2) incl += y;
+        }
+        const long long bb = base + (long long)(incl - nc) * a.Hkv;  // sequence bq's first chunk
+        const bool mine = nc > 0 && cur >= bb && cur < bb + (long long)nc * a.Hkv;
+        const uint32_t m = __ballot_sync(0xffffffffu, mine);
+        if (mine) {
+          const int hh = (int)((cur - bb) / nc);
+          const long long ps = bb + (long long)hh * nc, pe = ps + nc;
+          const long long e1 = hi < pe ? hi : pe;
+          const long long first_cta = ps / per, last_cta = (pe - 1) / per;
+          fl_unit[0] = bq;
+          fl_unit[1] = hh;
+          fl_unit[2] = (int)(cur - ps);
+          fl_unit[3] = (int)(e1 - ps);
+          fl_unit[4] = (int)((long long)blockIdx.x - first_cta);
+          fl_unit[5] = (long long)blockIdx.x == last_cta ? (int)(last_cta - first_cta + 1) : a.S;
+        }
+        if (m) {
+          found = true;
+          break;
+        }
+        base += (long long)__shfl_sync(0xffffffffu, incl, 31) * a.Hkv;
+      }
+      if (!found && lane == 0) {  // context lengths changed under the launch
+        flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
+        fl_stop = 1;
+      }
+    }
+    __syncthreads();
+    if (fl_stop) break;
+    b = fl_unit[0];
+    h = fl_unit[1];
+    c_first = fl_unit[2];
+    c_end = fl_unit[3];
+    s = fl_unit[4];
+    empty_from = fl_unit[5];
+  } else {
+    s = 0;
+    h = blockIdx.y;
+    b = mma::longest_first(a.context_lens, a.B, blockIdx.z);
+  }
+  do {  // one unit; early exits leave by break
   // With pos_split (more query rows than one CTA holds) a CTA serves the
   // pos_tile query positions j0 .. j0 + Tc - 1 of the sequence; position j
   // attends to the first L - T + 1 + j tokens (causal verify or extend), so
@@ -164,13 +286,9 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
   // order (x = split * tiles + tile): they read the same pages, so all but
   // the first read are mostly served by L2.
   const int n_tiles = a.pos_split ? (a.T + a.pos_tile - 1) / a.pos_tile : 1;
-  const int s = (int)blockIdx.x / n_tiles;
-  const int h = blockIdx.y, b = mma::longest_first(a.context_lens, a.B, blockIdx.z);
+  if (!FLAT) s = (int)blockIdx.x / n_tiles;
   const int j0 = a.pos_split ? ((int)blockIdx.x % n_tiles) * a.pos_tile : 0;
   const int Tc = a.pos_split ? min(a.pos_tile, a.T - j0) : a.T;  // query positions in this CTA
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int G = a.Hq / a.Hkv;
   const int R = Tc * G;
   const int L_seq = a.context_lens[b];
   const int L = a.causal ? L_seq - (a.T - Tc) + j0 : L_seq;  // tokens visible to this CTA's last position
@@ -189,24 +307,24 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
   if (L_seq < (a.causal ? a.T : 0) || L_seq > a.max_pages * kPage) {
     if (tid == 0 && s == 0 && h == 0) flag_error(a.dev_error, KV4_DEVERR_CONTEXT);
     write_empty();
-    return;
+    break;
   }
   const int n_pages = (L + kPage - 1) / kPage;
-  const int per = (n_pages + a.S - 1) / a.S;
-  const int p0 = s * per;
-  const int p1 = min(n_pages, p0 + per);
+  int p0, p1;
+  if constexpr (FLAT) {
+    p0 = c_first * kPagesPerChunk;
+    p1 = min(n_pages, c_end * kPagesPerChunk);
+  } else {
+    const int per = (n_pages + a.S - 1) / a.S;
+    p0 = s * per;
+    p1 = min(n_pages, p0 + per);
+  }
   if (p0 >= p1) {
     write_empty();
-    return;
+    break;
   }
   const int n_chunks = (p1 - p0 + kPagesPerChunk - 1) / kPagesPerChunk;
   const int32_t* table = a.block_tables + (size_t)b * a.max_pages;
-  uint64_t* bars = sm.bars();  // [kWarps][kStages]
-
-  // ---- barriers
-  if (lane == 0)
-    for (int i = 0; i < kStages; ++i) mbar_init(&bars[w * kStages + i], 1);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
   // Page ids of chunk c for lanes 0..3 (page 0 for lanes past the split; a
   // bad id is flagged and read as page 0).
@@ -256,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
   fence_proxy_async();
   for (int i = 0; i < kStages; ++i) {
     const int c = w + kWarps * i;
-    if (c < n_chunks) issue(c, i, chunk_page(c));
+    if (c < n_chunks) issue(c, (it_base + i) % kStages, chunk_page(c));
   }
 
   // ---- q prologue: rotate (fp32 butterfly), scale row by 2^sigma, split into f16 hi + lo
@@ -348,17 +466,16 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
 
   float* ktab = sm.ktab(w);
   uint32_t* vtab = sm.vtab(w);
-  const int first_limit = (a.diag & KV4_DIAG_EXPIRE_FIRST_WAIT) ? 0 : kSpinLimit;
   bool timed_out = false;
   int it_fail = 0;
 
   for (int c = w, it = 0; c < n_chunks; c += kWarps, ++it) {
-    const int st = it % kStages;
-    const uint32_t parity = (uint32_t)((it / kStages) & 1);
+    const int st = (it_base + it) % kStages;
+    const uint32_t parity = (uint32_t)(((it_base + it) / kStages) & 1);
     // page ids for the refill of this stage, loaded now to hide their latency
     const int cn = c + kWarps * kStages;
     const int next_page = cn < n_chunks ? chunk_page(cn) : 0;
-    if (!mbar_wait(&bars[w * kStages + st], parity, it == 0 ? first_limit : kSpinLimit)) {
+    if (!mbar_wait(&bars[w * kStages + st], parity, it_base + it == 0 ? first_limit : kSpinLimit)) {
       timed_out = true;
       it_fail = it;
       break;
@@ -674,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     if (lane == 0) flag_error(a.dev_error, KV4_DEVERR_TIMEOUT);
     for (int it = it_fail; it < it_fail + kStages; ++it)
       if (w + kWarps * it < n_chunks)
-        (void)mbar_wait(&bars[w * kStages + it % kStages], (uint32_t)((it / kStages) & 1));
+        (void)mbar_wait(&bars[w * kStages + (it_base + it) % kStages], (uint32_t)(((it_base + it) / kStages) & 1));
   }
 
   // ---- merge the 4 warps, one row block at a time: row l sums, then O scaled
@@ -725,6 +842,26 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
       if (lane == 0) a.part_lse[rr] = wsum > 0.0f ? (M + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
     }
   }
+  if constexpr (FLAT) {
+    // the unit's unused slots, by the CTA holding its last chunk
+    for (int r = w; r < R; r += kWarps)
+      for (int sl = empty_from; sl < a.S; ++sl) {
+        const size_t rr = row_index(r) * a.S + sl;
+        for (int d = lane; d < D; d += 32) a.part_o[rr * D + d] = 0.0f;
+        if (lane == 0) a.part_lse[rr] = -INFINITY;
+      }
+    if (timed_out) fl_stop = 1;
+  }
+  it_base += n_chunks > w ? (n_chunks - w + kWarps - 1) / kWarps : 0;
+  } while (0);
+  if constexpr (!FLAT) break;
+  // the next unit of this CTA's part, once every thread is done with the
+  // merge area (the stages) and this unit's shared values
+  fence_proxy_async();
+  __syncthreads();
+  if (tid == 0) fl_cur += fl_unit[3] - fl_unit[2];
+  __syncthreads();
+  }  // units
 }
 
 }  // namespace fast
@@ -742,10 +879,23 @@ constexpr int kSplitRows = 24;
 template <int RB>
 cudaError_t launch_rb(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
-  const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel<RB>, fast::smem_bytes(RB), smem_set);
+  const cudaError_t e = set_smem_limit_once(fast::decode_fp4_mma_kernel<RB, false>, fast::smem_bytes(RB), smem_set);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.S * (a.pos_split ? (a.T + a.pos_tile - 1) / a.pos_tile : 1), a.Hkv, a.B);
-  fast::decode_fp4_mma_kernel<RB><<<grid, fast::kThreads, fast::smem_bytes(RB), st>>>(a, kmap, vmap);
+  fast::decode_fp4_mma_kernel<RB, false><<<grid, fast::kThreads, fast::smem_bytes(RB), st>>>(a, kmap, vmap);
+  return cudaGetLastError();
+}
+
+// Flat mode: one wave of CTAs (every resident slot of every SM), each an equal
+// part of the step's chunks.
+cudaError_t launch_flat(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st) {
+  static std::atomic<unsigned long long> smem_set{0};
+  auto* kern = fast::decode_fp4_mma_kernel<1, true>;
+  const cudaError_t e = set_smem_limit_once(kern, fast::smem_bytes(1), smem_set);
+  if (e != cudaSuccess) return e;
+  const int grid = flat_grid_size();
+  if (grid < 1) return cudaErrorUnknown;
+  kern<<<grid, fast::kThreads, fast::smem_bytes(1), st>>>(a, kmap, vmap);
   return cudaGetLastError();
 }
 
@@ -755,7 +905,7 @@ cudaError_t launch_rb(const DecodeArgs& a, const CUtensorMap& kmap, const CUtens
 // G = 8) run in one CTA as 1-3 row blocks; more rows (longer verify blocks,
 // extend steps) are tiled over CTAs of kSplitRows rows' worth of whole
 // positions each (pos_split).
-cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st) {
+cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st, bool flat) {
   if (D != 128) return cudaErrorNotSupported;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
@@ -807,8 +957,29 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st) {
     a.pos_tile = kSplitRows / G > 0 ? kSplitRows / G : 1;
     R = a.pos_tile * G;
   }
+  if (flat) {
+    if (R > 8 || a.pos_split || a.S < 2 || !a.causal) return cudaErrorNotSupported;
+    return launch_flat(a, kmap, vmap, st);
+  }
   if (R <= 8) return launch_rb<1>(a, kmap, vmap, st);
   return R <= 16 ? launch_rb<2>(a, kmap, vmap, st) : launch_rb<3>(a, kmap, vmap, st);
+}
+
+bool flat_path_supported(int D, int G, int T, bool latent, int S) { return D == 128 && !latent && T * G <= 8 && S >= 2; }
+
+int flat_grid_size() {
+  static int grid = 0;
+  if (grid == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(fast::decode_fp4_mma_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             fast::smem_bytes(1)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fast::decode_fp4_mma_kernel<1, true>, fast::kThreads,
+                                                      fast::smem_bytes(1)) != cudaSuccess)
+      return 0;
+    grid = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  return grid;
 }
 
 }  // namespace kv4

@@ -147,7 +147,12 @@ size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int
  *                 to tokens t < context_lens[b] - q_per_seq + 1 + j.
  *   softmax_scale multiplies q.k before the softmax; finite and > 0, else
  *                 KV4_ERR_INVALID_ARG.
- *   num_splits    KV splits per sequence (0 = kv4_decode_auto_splits).
+ *   num_splits    KV splits per sequence: partial slots per (sequence, kv
+ *                 head), 0 = kv4_decode_auto_splits.  The split form cuts each
+ *                 sequence into num_splits equal parts; the flat mode (up to 8
+ *                 query rows per kv head) cuts the step's chunks into one
+ *                 wave of equal parts, of which a sequence's kv head spans at
+ *                 most num_splits.
  *   workspace     device, >= kv4_decode_workspace_bytes(...) bytes.
  *   out           device fp32 [batch][q_per_seq][num_q_heads][head_dim],
  *                 unrotated: out = softmax(s q.k) . v over the dequantised cache.
@@ -243,7 +248,8 @@ kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
 /* ---------------------------------------------------------------------
  * Kernel choice and test controls (diagnostics).
  *
- * kv4_decode_attention picks the split kernel from the shape alone.  This
+ * kv4_decode_attention picks the split kernel from the shape (and, for the
+ * flat mode, from num_splits and the device's SM count).  This
  * entry point is the same call with that choice made explicit, for tests and
  * measurements that compare the kernels on one input.  Every kernel computes
  * the same attention (the results differ by accumulation order, well inside
@@ -261,8 +267,11 @@ kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
                                   (T * num_q_heads / num_kv_heads <= 8) */
 #define KV4_KERNEL_LATENT_TC 6 /* warp-specialised tcgen05 latent (MLA) kernel: head_dim 512,
                                   K = V, <= 16 rows; one CTA per SM */
-#define KV4_KERNEL_BALANCED 7  /* balanced warp-MMA kernel: head_dim 128, <= 8 rows, num_splits >= 2,
-                                  not the prefix form; one CTA per SM, chunks shared by its warps */
+#define KV4_KERNEL_BALANCED 7  /* warp-MMA kernel in flat mode: head_dim 128, <= 8 rows, num_splits >= 2,
+                                  not the prefix form; one wave of CTAs, each an equal share of
+                                  the step's 64-token chunks in (sequence, kv head) order; a
+                                  sequence and kv head spans at most num_splits CTAs (its
+                                  partial slots) */
 
 /* Test controls (bits of diag_flags; 0 in normal use).
  * KV4_DIAG_EXPIRE_FIRST_WAIT: the first bounded wait of every warp that streams
@@ -281,6 +290,15 @@ kv4_status kv4_decode_attention_select(const void* q, const uint8_t* k_cache, co
                                        void* workspace, size_t workspace_bytes, float* out,
                                        int32_t* dev_error, int kernel, int diag_flags,
                                        kv4_stream_t stream);
+
+/* The KV4_KERNEL_* id that kv4_decode_attention (4-bit cache, causal form)
+ * would run for this shape with num_splits slots (>= 1; pass the value the
+ * call would use, e.g. kv4_decode_auto_splits) on the current device; latent
+ * != 0 for the latent cache (v_cache NULL or == k_cache).  -1 for an invalid
+ * shape.  Host only; it reads the device's SM count and the flat mode's
+ * occupancy once. */
+int kv4_decode_kernel_choice(int batch, int q_per_seq, int num_q_heads, int num_kv_heads, int head_dim,
+                             int num_splits, int latent);
 
 /* Log-sum-exp merge of split partials, then the inverse rotation:
  *   lse = log sum_s exp(lse_s);  O = sum_s exp(lse_s - lse) O_s;  out = H_D O.

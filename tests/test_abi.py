@@ -176,3 +176,16 @@ def test_kernel_choice_is_validated_before_launch(lib):
     import subprocess
     out = subprocess.run(["nm", "-D", "--undefined-only", kv4.LIB_PATH], capture_output=True, text=True).stdout
     assert "getenv" not in out
+
+
+def test_kernel_choice_query(lib):
+    assert kv4.kv4_decode_kernel_choice(0, 1, 64, 8, 128, 4) == -1          # no sequences
+    assert kv4.kv4_decode_kernel_choice(4, 1, 60, 8, 128, 4) == -1          # heads not a multiple
+    assert kv4.kv4_decode_kernel_choice(4, 1, 64, 8, 96, 4) == -1           # unsupported head_dim
+    assert kv4.kv4_decode_kernel_choice(8, 1, 16, 1, 512, 18, latent=True) == kv4.KV4_KERNEL_LATENT_TC
+    assert kv4.kv4_decode_kernel_choice(4, 512, 64, 8, 128, 1) == kv4.KV4_KERNEL_EXTEND
+    assert kv4.kv4_decode_kernel_choice(32, 3, 64, 8, 128, 4) == kv4.KV4_KERNEL_WARP_MMA   # 24 rows
+    assert kv4.kv4_decode_kernel_choice(4, 1, 80, 8, 128, 4) == kv4.KV4_KERNEL_GENERAL     # G = 10
+    # up to 8 rows: the flat mode where the slots fill a wave on this device, else the split form
+    assert kv4.kv4_decode_kernel_choice(32, 1, 64, 8, 128, 4) in (kv4.KV4_KERNEL_BALANCED, kv4.KV4_KERNEL_WARP_MMA)
+    assert kv4.kv4_decode_kernel_choice(32, 1, 64, 8, 128, 1) == kv4.KV4_KERNEL_WARP_MMA

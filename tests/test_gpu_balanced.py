@@ -1,12 +1,12 @@
-"""GPU parity of the balanced decode kernel (KV4_KERNEL_BALANCED: one CTA per
-SM takes an equal part of the flat (sequence, kv head, 4-page chunk) range and
-its warps pull chunks from it; "UltraQuant on AMD Instinct", section "Why
-UltraQuant beats 8-bit KV": a decode step is one stream over the whole cache)
-against the CPU oracle, and agreement with the warp-MMA split kernel on the
-same cache: short and ragged contexts (a CTA's part then crosses many
-(sequence, kv head) boundaries and is taken in several rounds of at most four
-segments), long ones, GQA groups of 4 and 8, two positions of 4 query heads,
-split slot counts 2 to 4, and pages shared by sequences."""
+"""GPU parity of the warp-MMA kernel's flat mode (KV4_KERNEL_BALANCED: one wave
+of CTAs, each an equal part of the flat (sequence, kv head, 4-page chunk)
+range, run as one unit per (sequence, kv head) it meets; "UltraQuant on AMD
+Instinct", section "Why UltraQuant beats 8-bit KV": a decode step is one
+stream over the whole cache) against the CPU oracle, and agreement with the
+split form on the same cache: short and ragged contexts (a CTA's part then
+crosses many (sequence, kv head) boundaries), many short sequences (parts of
+one or two chunks), long ones, GQA groups of 4 and 8, two positions of 4 query
+heads, split slot counts 2 to 4, and pages shared by sequences."""
 import dataclasses
 
 import numpy as np
@@ -26,6 +26,7 @@ CASES = {
     "tiny": W.CONFIGS["tiny"],                                     # G = 4, outliers x20
     "b32_small": W.scaled(_B32, batch=3, ctx=("fixed", 1000)),
     "ragged": W.scaled(_B32, batch=5, ctx=("uniform", 1, 900)),
+    "many_short": W.scaled(_B32, batch=48, ctx=("uniform", 1, 200)),
     "long": W.scaled(_B32, batch=2, ctx=("fixed", 4099)),
     "t2_g4": dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 50, 1300)), q_per_seq=2, num_q_heads=32),
     "shared": dataclasses.replace(W.scaled(_B32, batch=4, ctx=("uniform", 600, 3000)), shared_prefix=0.9),
@@ -71,3 +72,47 @@ def test_balanced_decode_refuses_other_shapes():
         kv4.kv4_decode_attention_select(W.queries(cfg).cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads,
                                         lay.num_pages, cfg.softmax_scale, kv4.KV4_KERNEL_BALANCED, num_splits=2)
     assert e.value.status == kv4.KV4_ERR_UNSUPPORTED
+
+
+def test_balanced_decode_flags_bad_inputs_and_keeps_the_rest():
+    """A page id out of range is flagged and read as page 0; a sequence whose
+    context length is out of range is flagged, takes no part of the flat range
+    and comes out as zeros, and the other sequences keep their result."""
+    cfg = W.scaled(_B32, batch=3, ctx=("fixed", 700))
+    lay = W.make_layout(cfg)
+    k, v, slots = all_tokens(cfg, lay)
+    gkc, gvc = gpu_caches(kv4, cfg, lay, k, v, slots)
+    tab, lens = gpu_tables(lay)
+    q = W.queries(cfg).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sel = lambda t_, l_: kv4.kv4_decode_attention_select(q, gkc, gvc, t_, l_, cfg.num_kv_heads, lay.num_pages,
+                                                          cfg.softmax_scale, kv4.KV4_KERNEL_BALANCED,
+                                                          num_splits=3, dev_error=err)
+    good = sel(tab, lens)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bad_tab = tab.clone()
+    bad_tab[1, 2] = lay.num_pages + 5
+    out = sel(bad_tab, lens)
+    torch.cuda.synchronize()
+    assert int(err.item()) & kv4.KV4_DEVERR_PAGE
+    assert torch.isfinite(out).all()
+    err.zero_()
+    bad_lens = lens.clone()
+    bad_lens[0] = lay.max_pages * cfg.page_size + 1
+    out = sel(tab, bad_lens)
+    torch.cuda.synchronize()
+    assert int(err.item()) & kv4.KV4_DEVERR_CONTEXT
+    assert (out[0] == 0).all()
+    # the other sequences' chunks are parted differently, so only the rounding differs
+    assert (out[1:] - good[1:]).abs().max().item() <= 2e-4
+
+
+def test_automatic_choice_takes_the_flat_mode_where_it_fills_a_wave():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # four resident CTAs per SM: batch 32 x 8 kv heads with 4 slots fills a wave
+    assert kv4.kv4_decode_kernel_choice(32, 1, 64, 8, 128, 4) == (kv4.KV4_KERNEL_BALANCED if 3 * 256 >= 4 * sms
+                                                                  else kv4.KV4_KERNEL_WARP_MMA)
+    # 2 slots for 64 sequences: a part per sequence is too few for the wave
+    assert kv4.kv4_decode_kernel_choice(64, 1, 64, 8, 128, 2) == (kv4.KV4_KERNEL_BALANCED if 512 >= 4 * sms
+                                                                  else kv4.KV4_KERNEL_WARP_MMA)
