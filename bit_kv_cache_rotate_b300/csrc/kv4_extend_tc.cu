@@ -525,7 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
     }
     // ---- V' (dim tid % 128, pages 4h .. 4h + 3 of the chunk) -> canonical K-major tile
-    if (!timed_out) {
+    // (the f16 and bf16 forms as separate loops: one branch per chunk)
+    auto widen_v = [&](auto wide_t) {
+      constexpr bool kWide = decltype(wide_t)::value;
       const int d = tid & (D - 1), g4 = d >> 5;
       const uint8_t* vr = smem + kOffVR + rb * kVR + d * 8;
       const uint4* fr = reinterpret_cast<const uint4*>(fac + g4 * kChunk);
@@ -538,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t word = hh ? wv.y : wv.x;
           const uint4 f = fr[pi * 2 + hh];
           uint4 o;
-          if (!wide) {
+          if (!kWide) {
             o.x = hmul2(e2m1x2_to_f16x2(word, 0), f.x);
             o.y = hmul2(e2m1x2_to_f16x2(word, 1), f.y);
             o.z = hmul2(e2m1x2_to_f16x2(word, 2), f.z);
@@ -552,6 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(smem + kOffVF + ((d >> 3) * 16 + pi * 2 + hh) * 128 + (d & 7) * 16) = o;
         }
       }
+    };
+    if (!timed_out) {
+      if (wide) widen_v(std::true_type{});
+      else widen_v(std::false_type{});
     }
     // ---- S of the chunk
     if (!mbar_wait(&sdone[c & 1], (uint32_t)((c >> 1) & 1))) timed_out = true;
@@ -600,8 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float shift = m_new == -INFINITY ? -INFINITY : (float)(e_x - e_ref) - m_new;
     const float2 sh2 = make_float2(shift, shift);
     float2 ls2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-    auto write_p = [&](auto masked) {
+    auto write_p = [&](auto masked, auto wide_t) {
       constexpr bool M = decltype(masked)::value;
+      constexpr bool kWide = decltype(wide_t)::value;
 #pragma unroll 1
       for (int q = 0; q < 2; ++q) {
         uint32_t sv[32];
@@ -622,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 t = __fadd2_rn(x, sh2);
             const float2 pp = make_float2(ex2(t.x), ex2(t.y));
             ls2[i2 & 1] = __fadd2_rn(ls2[i2 & 1], pp);
-            if (!wide) {
+            if (!kWide) {
               hw[i2] = pack_f16x2(pp.x, pp.y);
               const float2 hf2 = __half22float2(*reinterpret_cast<const __half2*>(&hw[i2]));
               const float2 lo = __fadd2_rn(pp, make_float2(-hf2.x, -hf2.y));
@@ -639,8 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     if (!timed_out) {
-      if (all_full) write_p(std::false_type{});
-      else write_p(std::true_type{});
+      if (!wide) {
+        if (all_full) write_p(std::false_type{}, std::false_type{});
+        else write_p(std::true_type{}, std::false_type{});
+      } else {
+        if (all_full) write_p(std::false_type{}, std::true_type{});
+        else write_p(std::true_type{}, std::true_type{});
+      }
     }
     const float lsum = (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
     // l in the units of p (not p'): p = p' * 2^(E_ref - E_x), E_ref - E_x in [-4, 30]
