@@ -144,6 +144,17 @@ __device__ __forceinline__ void pv_bf16(float (&o)[RB][8][4], const float2 (&p)[
   }
 }
 
+// Share of a row's running sum above which a token keeps the lo part of P:
+// 2^-4 while every V group reference is at most 2^1 (|v| < 12), a quarter of
+// that per binade above, so the error the other tokens' f16 rounding leaves
+// (about 2^-11 |v| sqrt(share)) stays the same for any V magnitude.
+__device__ __forceinline__ float lo_share_of(uint32_t eref) {
+  uint32_t em = __vmaxu4(eref, eref >> 16);
+  em = max(em & 0xFFu, (em >> 8) & 0xFFu);
+  const int k = min(120, 4 + 2 * max(0, (int)em - 128));
+  return __uint_as_float((uint32_t)(127 - k) << 23);
+}
+
 // ---------------------------------------------------------------- kernel
 // Rows: the R = T*G query rows of one kv head, R <= 8 * RB (row r -> position
 // r / G, query head h*G + r % G), in RB blocks of 8 MMA rows; unused rows
@@ -463,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
     l2[rb] = make_float2(0.0f, 0.0f);
   }
   uint32_t eref = 0;  // 4 UE8M0 bytes: running max of V exponents per group
+  float lo_share = 0.0625f;  // the lo part of P's share threshold for this eref
 
   float* ktab = sm.ktab(w);
   uint32_t* vtab = sm.vtab(w);
@@ -515,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
 #pragma unroll
         for (int o2 = 16; o2 >= 1; o2 >>= 1) cm = __vmaxu4(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
         eref = __vmaxu4(eref, cm);
+        lo_share = lo_share_of(eref);
         lim = __vaddus4(eref, 0x07070707u);
       }
       // K scale pairs: {2^e(tk,G), 2^e(tk+1,G)} for G = 0..3 (byte 0 -> 0.0)
@@ -684,9 +697,18 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
 
     // ---- P fragments (hi + lo f16): k-step c4 uses tokens 4c4..4c4+3 of page t.
     // hi is p rounded to f16, lo the exact fp32 remainder p - hi rounded to f16.
-    // The lo part matters only for large p: its MMAs run for a k-step only when
-    // some p of the step (any row, any page) exceeds 2^-8; below that the f16
-    // rounding of p alone stays under 2^-20 per token.
+    // The lo part matters only for a token that carries a noticeable share of
+    // its row: its MMAs run for a k-step only when some p of the step (any row,
+    // any page) exceeds tau times its row's running sum in this warp.  Every
+    // other token keeps p rounded to f16 (relative error at most 2^-11); those
+    // errors enter the output weighted by p / l, each weight below tau, and
+    // add up like independent roundings: about 2^-11 |v| times the root of the
+    // sum of the squared weights, at most sqrt(tau).  tau = 2^-4 while |v| <
+    // 12 (largest V group reference 2^1) puts that near 2^-11 * 12 / 4 = 1.5e-3
+    // in the worst case and measures 1e-4 to 5e-4 on the workloads and stress
+    // cases; tau falls by 4 per binade of larger V (lo_share_of) so the bound
+    // holds for any V magnitude.  In a long context every token's weight is
+    // far below tau and the lo MMAs are skipped; a short one keeps them.
     const uint8_t* vbase = stg + kPagesPerChunk * kBlkStride + t * kVStride;
     if (__any_sync(0xffffffffu, under)) {
       // The reference is re-taken from the chunk itself: each group's largest
@@ -718,13 +740,24 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
             for (int k4 = 0; k4 < 4; ++k4) o[rb][2 * G4 + jj][k4] *= f;
       }
       eref = enew;
+      lo_share = lo_share_of(eref);
       pv_bf16<RB>(o, p, vbase, eref, g);
     } else {
     uint32_t ph[RB][4][2], pl[RB][4][2];
     bool need_lo[4];
+    // lo matters for a token above a share (lo_share) of its row's running
+    // sum in this warp, this chunk included
+    float lo_thr[RB];
+#pragma unroll
+    for (int rb = 0; rb < RB; ++rb) {
+      float lr = l2[rb].x + l2[rb].y;
+      lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+      lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+      lo_thr[rb] = lo_share * lr;
+    }
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
-      float pm = 0.0f;
+      bool big = false;
 #pragma unroll
       for (int rb = 0; rb < RB; ++rb) {
         ph[rb][c4][0] = pack_f16x2(p[rb][2 * c4].x, p[rb][2 * c4].y);
@@ -735,9 +768,10 @@ __global__ void __launch_bounds__(kThreads, RB == 1 ? 4 : 2)
         const float2 l1 = __fadd2_rn(p[rb][2 * c4 + 1], make_float2(-h1.x, -h1.y));
         pl[rb][c4][0] = pack_f16x2(l0.x, l0.y);
         pl[rb][c4][1] = pack_f16x2(l1.x, l1.y);
-        pm = fmaxf(pm, fmaxf(fmaxf(p[rb][2 * c4].x, p[rb][2 * c4].y), fmaxf(p[rb][2 * c4 + 1].x, p[rb][2 * c4 + 1].y)));
+        const float pm = fmaxf(fmaxf(p[rb][2 * c4].x, p[rb][2 * c4].y), fmaxf(p[rb][2 * c4 + 1].x, p[rb][2 * c4 + 1].y));
+        big |= pm > lo_thr[rb];
       }
-      need_lo[c4] = __any_sync(0xffffffffu, pm > 0.00390625f);
+      need_lo[c4] = __any_sync(0xffffffffu, big);
     }
 
     // ---- P.V: m-tile j = dims 16j..16j+15 (group j/2); rows g, g+8 -> dims 16j+g, 16j+g+8.

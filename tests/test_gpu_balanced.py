@@ -59,7 +59,9 @@ def test_balanced_decode_parity(name):
         got = _run(cfg, lay, gkc, gvc, q, S, kv4.KV4_KERNEL_BALANCED)
         assert np.isfinite(got).all()
         assert np.abs(got - ref).max() <= TOL, (S, np.abs(got - ref).max())
-        assert np.abs(got - warp).max() <= 2e-4, (S, np.abs(got - warp).max())
+        # the two forms give different tokens to a warp's running row sum, so
+        # different tokens keep the lo part of P (f16 rounding, 2^-11 relative)
+        assert np.abs(got - warp).max() <= 1e-3, (S, np.abs(got - warp).max())
 
 
 def test_balanced_decode_refuses_other_shapes():
@@ -105,7 +107,7 @@ def test_balanced_decode_flags_bad_inputs_and_keeps_the_rest():
     assert int(err.item()) & kv4.KV4_DEVERR_CONTEXT
     assert (out[0] == 0).all()
     # the other sequences' chunks are parted differently, so only the rounding differs
-    assert (out[1:] - good[1:]).abs().max().item() <= 2e-4
+    assert (out[1:] - good[1:]).abs().max().item() <= 1e-3
 
 
 def test_automatic_choice_takes_the_flat_mode_where_it_fills_a_wave():

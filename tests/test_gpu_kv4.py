@@ -92,8 +92,11 @@ def test_decode_split_count_invariance():
         got, ref = _decode_pair(cfg, lay, okc, ovc, gkc, gvc, q, num_splits=S)
         assert np.abs(got - ref).max() <= TOL, S
         outs.append(got)
+    # Split counts change which tokens share a warp's running row sum, and so
+    # which tokens keep the lo part of P (a token above a share of that sum);
+    # the others' f16 rounding of p (2^-11 relative) differs between counts.
     for o in outs[1:]:
-        assert np.abs(o - outs[0]).max() <= 1e-4
+        assert np.abs(o - outs[0]).max() <= 1e-3
 
 
 @pytest.mark.parametrize("ctx", [1, 3, 15, 16, 17, 33])
@@ -267,3 +270,42 @@ def test_mla_latent_decode_ragged_and_split_invariant(ctx):
         outs.append(got)
     for o in outs[1:]:
         assert np.abs(o - outs[0]).max() <= 1e-4
+
+
+def test_decode_with_moderately_dominant_tokens():
+    """Rows whose weight sits on a few hundred tokens of a few tenths of a
+    percent to a percent each (keys pushed along the query), with values four
+    times the workload's: the warp-MMA kernel keeps the lo part of P only for
+    tokens above a share of a row's running sum (smaller for larger V), and
+    the rest (f16 rounding of p) must still stay within the parity
+    tolerance."""
+    cfg = W.scaled(W.CONFIGS["b32_ctx8k"], batch=2, ctx=("fixed", 3000))
+    lay = W.make_layout(cfg)
+    k, v, slots = all_tokens(cfg, lay)
+    q = W.queries(cfg)
+    G, L = cfg.group, 3000
+    gen = torch.Generator().manual_seed(7)
+    k = k.float()
+    for b in range(cfg.batch):
+        base = b * L  # no shared prefix: sequence b's tokens are rows b*L .. b*L + L - 1, in order
+        for h in range(cfg.num_kv_heads):
+            qh = q[b, 0, h * G].float()
+            qhat = qh / qh.norm()
+            idx = torch.randperm(L, generator=gen)[:248]
+            k[base + idx[:48], h] += 5.0 * qhat      # about 1 % of the row each
+            k[base + idx[48:], h] += 3.5 * qhat      # just under 2^-8 of the row each
+    k = k.to(torch.bfloat16)
+    v = (v.float() * 4.0).to(torch.bfloat16)
+    okc, ovc = oracle_caches(cfg, lay, k, v, slots)
+    gkc, gvc = gpu_caches(kv4, cfg, lay, k, v, slots)
+    tab, lens = gpu_tables(lay)
+    ref = oracle.decode_attention(q, okc, ovc, np.where(lay.block_tables < 0, 0, lay.block_tables),
+                                  lay.context_lens, cfg.num_kv_heads, cfg.page_size, lay.num_pages,
+                                  cfg.softmax_scale)
+    for kernel, S in ((kv4.KV4_KERNEL_AUTO, 0), (kv4.KV4_KERNEL_WARP_MMA, 1), (kv4.KV4_KERNEL_WARP_MMA, 3),
+                      (kv4.KV4_KERNEL_BALANCED, 4)):
+        out = kv4.kv4_decode_attention_select(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
+                                              cfg.softmax_scale, kernel, num_splits=S)
+        torch.cuda.synchronize()
+        e = np.abs(out.cpu().numpy().astype(np.float64) - ref).max()
+        assert e <= TOL, (kernel, S, e)

@@ -55,7 +55,9 @@ def test_tcgen05_decode_parity(name):
         got = _run(cfg, lay, gkc, gvc, q, S, kv4.KV4_KERNEL_TCGEN05)
         assert np.isfinite(got).all()
         assert np.abs(got - ref).max() <= TOL, (S, np.abs(got - ref).max())
-        assert np.abs(got - warp).max() <= 2e-4, (S, np.abs(got - warp).max())
+        # the kernels keep the lo part of P for different tokens (f16 rounding of
+        # the rest, 2^-11 relative)
+        assert np.abs(got - warp).max() <= 1e-3, (S, np.abs(got - warp).max())
 
 
 def test_tcgen05_decode_refuses_more_than_eight_rows():
