@@ -148,12 +148,14 @@ size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int
 // flat mode (one wave of CTAs over equal parts of the step's chunks) when the
 // S slots allow a wave's worth of equal parts of sequences of the table's full
 // length: (S - 1) x units >= the wave's CTAs; otherwise (few slots for many
-// sequences) the split form.
+// sequences) the split form.  With more rows (a verify block) the flat mode
+// measured slower (two CTAs per SM, its parts cross the shared prefix at
+// different times) and is an explicit choice only.
 static int auto_kernel(bool fp8, int D, int G, int T, bool latent, bool causal, int S, long long units) {
   if (!fp8 && kv4::extend_tc_supported(D, G, T, latent) && T * G > 4 * kv4::kTileRows) return KV4_KERNEL_EXTEND;
   if (!fp8 && kv4::mla_tc_path_supported(D, G, T, latent)) return KV4_KERNEL_LATENT_TC;
-  if (!fp8 && causal && kv4::flat_path_supported(D, G, T, latent, S)) {
-    const int grid = kv4::flat_grid_size();
+  if (!fp8 && causal && T * G <= 8 && kv4::flat_path_supported(D, G, T, latent, S)) {
+    const int grid = kv4::flat_grid_size(T * G);
     if (grid > 0 && (long long)(S - 1) * units >= grid) return KV4_KERNEL_BALANCED;
   }
   const bool ok_warp = fp8 ? kv4::fp8_fast_path_supported(D, G, T) : kv4::fast_path_supported(D, G, T, latent);

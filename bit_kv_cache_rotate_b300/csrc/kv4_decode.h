@@ -50,15 +50,16 @@ inline int choose_splits(int units, int max_pages, int head_dim, int sms) {
 
 cudaError_t launch_decode_ref(bool fp8, int D, const DecodeArgs& a, cudaStream_t st);
 bool fast_path_supported(int D, int G, int T, bool latent);
-// flat: one wave of CTAs over equal parts of the step's chunks (T * G <= 8,
+// flat: one wave of CTAs over equal parts of the step's chunks (T * G <= 24,
 // causal, S >= 2 slots per sequence and kv head); else the split form.
 cudaError_t launch_decode_fast(int D, const DecodeArgs& a, cudaStream_t st, bool flat = false);
 bool mla_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st);
 bool mla_tc_path_supported(int D, int G, int T, bool latent);
 bool flat_path_supported(int D, int G, int T, bool latent, int S);
-// CTAs of the flat mode's launch: every resident slot of every SM (0 on error).
-int flat_grid_size();
+// CTAs of the flat mode's launch for `rows` query rows per kv head: every
+// resident slot of every SM (0 on error).
+int flat_grid_size(int rows);
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, cudaStream_t st);
 bool tc_path_supported(int D, int G, int T, bool latent);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);

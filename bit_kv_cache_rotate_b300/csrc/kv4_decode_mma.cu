@@ -922,15 +922,31 @@ cudaError_t launch_rb(const DecodeArgs& a, const CUtensorMap& kmap, const CUtens
 
 // Flat mode: one wave of CTAs (every resident slot of every SM), each an equal
 // part of the step's chunks.
+template <int RB>
 cudaError_t launch_flat(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t st) {
   static std::atomic<unsigned long long> smem_set{0};
-  auto* kern = fast::decode_fp4_mma_kernel<1, true>;
-  const cudaError_t e = set_smem_limit_once(kern, fast::smem_bytes(1), smem_set);
+  auto* kern = fast::decode_fp4_mma_kernel<RB, true>;
+  const cudaError_t e = set_smem_limit_once(kern, fast::smem_bytes(RB), smem_set);
   if (e != cudaSuccess) return e;
-  const int grid = flat_grid_size();
+  const int grid = flat_grid_size(8 * RB);
   if (grid < 1) return cudaErrorUnknown;
-  kern<<<grid, fast::kThreads, fast::smem_bytes(1), st>>>(a, kmap, vmap);
+  kern<<<grid, fast::kThreads, fast::smem_bytes(RB), st>>>(a, kmap, vmap);
   return cudaGetLastError();
+}
+
+template <int RB>
+int flat_grid_of() {
+  static int grid = 0;
+  if (grid == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    auto* kern = fast::decode_fp4_mma_kernel<RB, true>;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fast::smem_bytes(RB)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, fast::kThreads, fast::smem_bytes(RB)) != cudaSuccess)
+      return 0;
+    grid = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  return grid;
 }
 
 }  // namespace
@@ -992,28 +1008,21 @@ cudaError_t launch_decode_fast(int D, const DecodeArgs& a_in, cudaStream_t st, b
     R = a.pos_tile * G;
   }
   if (flat) {
-    if (R > 8 || a.pos_split || a.S < 2 || !a.causal) return cudaErrorNotSupported;
-    return launch_flat(a, kmap, vmap, st);
+    if (a.pos_split || a.S < 2 || !a.causal) return cudaErrorNotSupported;
+    if (R <= 8) return launch_flat<1>(a, kmap, vmap, st);
+    return R <= 16 ? launch_flat<2>(a, kmap, vmap, st) : launch_flat<3>(a, kmap, vmap, st);
   }
   if (R <= 8) return launch_rb<1>(a, kmap, vmap, st);
   return R <= 16 ? launch_rb<2>(a, kmap, vmap, st) : launch_rb<3>(a, kmap, vmap, st);
 }
 
-bool flat_path_supported(int D, int G, int T, bool latent, int S) { return D == 128 && !latent && T * G <= 8 && S >= 2; }
+bool flat_path_supported(int D, int G, int T, bool latent, int S) {
+  return D == 128 && !latent && T * G <= kTileRows && S >= 2;
+}
 
-int flat_grid_size() {
-  static int grid = 0;
-  if (grid == 0) {
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(fast::decode_fp4_mma_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             fast::smem_bytes(1)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fast::decode_fp4_mma_kernel<1, true>, fast::kThreads,
-                                                      fast::smem_bytes(1)) != cudaSuccess)
-      return 0;
-    grid = sms * (per_sm > 0 ? per_sm : 1);
-  }
-  return grid;
+int flat_grid_size(int rows) {
+  if (rows <= 8) return flat_grid_of<1>();
+  return rows <= 16 ? flat_grid_of<2>() : flat_grid_of<3>();
 }
 
 }  // namespace kv4

@@ -149,7 +149,7 @@ size_t kv4_decode_workspace_bytes(int batch, int q_per_seq, int num_q_heads, int
  *                 KV4_ERR_INVALID_ARG.
  *   num_splits    KV splits per sequence: partial slots per (sequence, kv
  *                 head), 0 = kv4_decode_auto_splits.  The split form cuts each
- *                 sequence into num_splits equal parts; the flat mode (up to 8
+ *                 sequence into num_splits equal parts; the flat mode (up to 24
  *                 query rows per kv head) cuts the step's chunks into one
  *                 wave of equal parts, of which a sequence's kv head spans at
  *                 most num_splits.
@@ -267,7 +267,7 @@ kv4_status kv4_decode_attention_noalloc(const void* q, const uint8_t* k_cache,
                                   (T * num_q_heads / num_kv_heads <= 8) */
 #define KV4_KERNEL_LATENT_TC 6 /* warp-specialised tcgen05 latent (MLA) kernel: head_dim 512,
                                   K = V, <= 16 rows; one CTA per SM */
-#define KV4_KERNEL_BALANCED 7  /* warp-MMA kernel in flat mode: head_dim 128, <= 8 rows, num_splits >= 2,
+#define KV4_KERNEL_BALANCED 7  /* warp-MMA kernel in flat mode: head_dim 128, <= 24 rows, num_splits >= 2,
                                   not the prefix form; one wave of CTAs, each an equal share of
                                   the step's 64-token chunks in (sequence, kv head) order; a
                                   sequence and kv head spans at most num_splits CTAs (its

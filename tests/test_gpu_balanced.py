@@ -29,6 +29,8 @@ CASES = {
     "many_short": W.scaled(_B32, batch=48, ctx=("uniform", 1, 200)),
     "long": W.scaled(_B32, batch=2, ctx=("fixed", 4099)),
     "t2_g4": dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 50, 1300)), q_per_seq=2, num_q_heads=32),
+    "verify_t3": W.scaled(W.CONFIGS["verify_agentic"], batch=4, ctx=("uniform", 300, 1500)),   # 24 rows
+    "t2_g8": dataclasses.replace(W.scaled(_B32, batch=3, ctx=("uniform", 50, 1300)), q_per_seq=2),  # 16 rows
     "shared": dataclasses.replace(W.scaled(_B32, batch=4, ctx=("uniform", 600, 3000)), shared_prefix=0.9),
 }
 
@@ -65,7 +67,7 @@ def test_balanced_decode_parity(name):
 
 
 def test_balanced_decode_refuses_other_shapes():
-    cfg = W.scaled(W.CONFIGS["verify_agentic"], batch=1, ctx=("fixed", 100))   # 24 rows
+    cfg = W.scaled(W.CONFIGS["verify6_agentic"], batch=1, ctx=("fixed", 100))   # 48 rows
     lay = W.make_layout(cfg)
     k, v, slots = all_tokens(cfg, lay)
     gkc, gvc = gpu_caches(kv4, cfg, lay, k, v, slots)
