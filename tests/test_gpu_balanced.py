@@ -120,3 +120,44 @@ def test_automatic_choice_takes_the_flat_mode_where_it_fills_a_wave():
     # 2 slots for 64 sequences: a part per sequence is too few for the wave
     assert kv4.kv4_decode_kernel_choice(64, 1, 64, 8, 128, 2) == (kv4.KV4_KERNEL_BALANCED if 512 >= 4 * sms
                                                                   else kv4.KV4_KERNEL_WARP_MMA)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_balanced_decode_random_shapes_write_every_slot(seed):
+    """Seeded random batches (sizes, context mixes, GQA groups, positions and
+    slot counts): the flat mode's parts, units and empty slots must cover
+    every partial the combine reads -- the workspace starts as NaN, so a
+    partial left unwritten would reach the output -- and agree with the oracle
+    and the split form."""
+    rng = np.random.default_rng(1000 + seed)
+    G = int(rng.choice([1, 2, 4, 8]))
+    T = int(rng.choice([t for t in (1, 2, 3) if t * G <= 24]))
+    Hkv = int(rng.choice([1, 2, 3, 8]))
+    batch = int(rng.integers(1, 40))
+    hi = int(rng.choice([40, 300, 2000]))
+    cfg = dataclasses.replace(W.scaled(_B32, batch=batch, ctx=("uniform", T, max(T + 1, hi)),
+                                       name=f"rand{seed}"),
+                              num_kv_heads=Hkv, num_q_heads=Hkv * G, q_per_seq=T)
+    S = int(rng.integers(2, 9))
+    lay = W.make_layout(cfg)
+    k, v, slots = all_tokens(cfg, lay)
+    okc, ovc = oracle_caches(cfg, lay, k, v, slots)
+    gkc, gvc = gpu_caches(kv4, cfg, lay, k, v, slots)
+    q = W.queries(cfg)
+    tab, lens = gpu_tables(lay)
+    ws = kv4.workspace(cfg.batch, T, cfg.num_q_heads, cfg.head_dim, S)
+    ws.view(torch.float32).fill_(float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kv4.kv4_decode_attention_select(q.cuda(), gkc, gvc, tab, lens, cfg.num_kv_heads, lay.num_pages,
+                                          cfg.softmax_scale, kv4.KV4_KERNEL_BALANCED, num_splits=S,
+                                          workspace_buf=ws, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all(), (G, T, Hkv, batch, hi, S)
+    ref = oracle.decode_attention(q, okc, ovc, np.where(lay.block_tables < 0, 0, lay.block_tables),
+                                  lay.context_lens, cfg.num_kv_heads, cfg.page_size, lay.num_pages,
+                                  cfg.softmax_scale)
+    assert np.abs(got - ref).max() <= TOL, (G, T, Hkv, batch, hi, S, np.abs(got - ref).max())
+    split = _run(cfg, lay, gkc, gvc, q, S, kv4.KV4_KERNEL_WARP_MMA)
+    assert np.abs(got - split).max() <= 1e-3
