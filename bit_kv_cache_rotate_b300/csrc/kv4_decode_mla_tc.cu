@@ -31,7 +31,7 @@
 // Warp roles, one CTA per (split, latent head, sequence), 10 warps, one CTA
 // per SM (all of tensor memory):
 //   warps 0-3  softmax: thread = token 32w + lane of the chunk; places the
-//              chunk's scales of A, loads its logits, runs the online softmax
+//              scales of A two chunks ahead, loads the logits, runs the online softmax
 //              (a lazy maximum shared by the four warps), rescales the
 //              accumulated O^T when a reference moved, writes P^T, computes the
 //              next chunk's V factors; at the end reads O^T (channels 32w +
@@ -828,13 +828,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     // (the abort flag ends every other wait at once) and the next barrier,
     // where all four warps take part, turns it into a common exit.
     ok = place_sfa(0, true);
+    if (n_chunks > 1) ok = place_sfa(1, ok);
     ok = publish_ref(0, ok);
     ok = !bar_or(1, kSmWarps * 32, !ok);
     bool good = true;
     for (int c = 0; c < n_chunks && ok; ++c) {
       const int st = c % kStages, bb = c & 1;
       // ---- scales of A for chunk c + 1 (its Q.K^T runs while this chunk's softmax does)
-      if (c + 1 < n_chunks) good = place_sfa(c + 1, good);
       // ---- logits of this token: column 16i + r holds term pairs (2p + i) of row r
       good = good && wait_or_abort(&bars[kBarSFull + bb], (uint32_t)((c >> 1) & 1), abort_flag);
       if (!good && lane == 0) *abort_flag = 1;
@@ -977,6 +977,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       if (good && lane == 0) mbar_arrive(&bars[kBarP + bb]);
       // ---- V factors of chunk c + 1 (the converters start on it)
       if (c + 1 < n_chunks) good = publish_ref(c + 1, good);
+      // ---- scales of A for chunk c + 2 (buffer c % 2: Q.K^T of chunk c is
+      // done), so its Q.K^T runs while chunk c + 1's softmax does
+      if (c + 2 < n_chunks) good = place_sfa(c + 2, good);
       if (!good && lane == 0) *abort_flag = 1;
     }
     ok = ok && good;
