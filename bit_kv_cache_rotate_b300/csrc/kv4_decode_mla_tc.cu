@@ -20,22 +20,20 @@
 //          the same columns: 32 MMAs per chunk.
 //   P.V    O^T[channel][row] = V'^T P^T, M = 128 channels (four blocks), N =
 //          16 rows, K = 16 tokens per MMA, kind::f16.  A = V' = code * 2^(e -
-//          E_g), E_g the running largest exponent of the channel group (chunks
-//          so far), widened once per chunk by the converter warps (exact in f16
-//          from 23 binades below E_g; a chunk whose scales reach further takes
-//          bf16 V' and P); B = P as f16 hi + remainder (two MMAs per k-step).
-//          O^T accumulates in tensor memory over all chunks; when a row's
-//          softmax reference or a group's E_g moves with a chunk, the softmax
-//          warps rescale it in place before that chunk's P.V.
+//          E_c), E_c the chunk's largest exponent of the channel group, widened
+//          once per chunk by the converter warps (exact in f16 from 23 binades
+//          below E_c; a chunk whose scales span more takes bf16 V' and P);
+//          B = P as f16 hi + remainder (two MMAs per k-step).  Each chunk's O^T
+//          starts afresh in tensor memory and is added into the running O
+//          (registers, fp32) with the softmax and group-reference factors.
 //
 // Warp roles, one CTA per (split, latent head, sequence), 10 warps, one CTA
 // per SM (all of tensor memory):
 //   warps 0-3  softmax: thread = token 32w + lane of the chunk; places the
-//              scales of A two chunks ahead, loads the logits, runs the online softmax
-//              (a lazy maximum shared by the four warps), rescales the
-//              accumulated O^T when a reference moved, writes P^T, computes the
-//              next chunk's V factors; at the end reads O^T (channels 32w +
-//              lane of each block) and writes its channels.
+//              chunk's scales of A, loads its logits, runs the online softmax
+//              (a lazy maximum shared by the four warps), writes P^T, computes
+//              the chunk's V factors, and folds O^T (channels 32w + lane of
+//              each block) into registers; at the end writes its channels.
 //   warps 4-7  converters: V' of the chunk, 32 tokens at a time, into two
 //              alternating tiles (E2M1 -> f16 conversion times the factor,
 //              stored token by token: the tile is MN-major).
@@ -111,12 +109,12 @@ constexpr int kOffP = kOffVp + 2 * kVpBytes;                     // 202752
 // [2 chunks][128 tokens][16 groups]
 constexpr int kFacBytes = kChunk * kGroups * 2;                  // 4096
 constexpr int kOffFac = kOffP + 2 * kPBuf;
-// chunk references: [4 chunks][4 words of group exponents E, wide flag,
-// rose flag (a group's E moved up with the chunk), 2 spare]
+// chunk references: [4 chunks][4 words of group exponents E, flags (bit 0:
+// wide), 3 spare]
 constexpr int kRefRing = 4;
 constexpr int kOffRef = kOffFac + 2 * kFacBytes;
 // softmax warps' exchange words: [4 warps][16] group bytes and masks, [4
-// warps][16] row maxima or sums, [3][16] spare
+// warps][16] row maxima or sums, [3 chunks][16] the rows' softmax factors
 constexpr int kXchWords = 2 * kSmWarps * 16 + 3 * kRows;
 constexpr int kOffXch = kOffRef + kRefRing * 8 * 4;
 constexpr int kOffBar = kOffXch + kXchWords * 4;
@@ -137,8 +135,8 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;      // S: [2 buffers][32]
 constexpr uint32_t kColSfa = 64;   // scales of A: [2 buffers][8 k-steps][4]
 constexpr uint32_t kColSfb = 128;  // scales of B: [4 passes][8 k-steps][4]
-constexpr uint32_t kColO = 256;    // O^T accumulated over the chunks: [4 channel blocks][16 rows]
-constexpr int kOBufs = 3;          // P.V completion barriers (a ring by chunk)
+constexpr uint32_t kColO = 256;    // O^T of a chunk: [3 buffers][4 channel blocks][16 rows]
+constexpr int kOBufs = 3;
 
 // barriers
 constexpr int kBarFull = 0;        // [3] a chunk's copies landed (expect_tx)
@@ -151,7 +149,7 @@ constexpr int kBarP = 16;          // [2] P^T written (4)
 constexpr int kBarVpFull = 18;     // [2] a V' tile written (4)
 constexpr int kBarVpEmpty = 20;    // [2] the MMAs reading a V' tile done (commit)
 constexpr int kBarPv = 22;         // [3] P.V of a chunk done (commit)
-                                   // 25 .. 27 spare
+constexpr int kBarOEmpty = 25;     // [3] O^T of a chunk loaded (4)
 constexpr int kBarCvDone = 28;     // [4] converter warps done with a chunk (4)
 constexpr int kBarDrain = 32;      // [2] every MMA a warp issued done (after a timeout)
 constexpr int kBarRefStats = 34;   // [4] a chunk's group references and wide flag written (1)
@@ -374,7 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       mbar_init(&bars[kBarVpEmpty + i], 1);
       mbar_init(&bars[kBarDrain + i], 1);
     }
-    for (int i = 0; i < kOBufs; ++i) mbar_init(&bars[kBarPv + i], 1);
+    for (int i = 0; i < kOBufs; ++i) {
+      mbar_init(&bars[kBarPv + i], 1);
+      mbar_init(&bars[kBarOEmpty + i], kSmWarps);
+    }
     for (int i = 0; i < kRefRing; ++i) {
       mbar_init(&bars[kBarRefReady + i], kSmWarps);
       mbar_init(&bars[kBarCvDone + i], kCvWarps);
@@ -564,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     bool ok = true;
     for (int x = 0; x < n_chunks && ok; ++x) {
       const int bx = x & 1, ob = x % kOBufs;
-      ok = wait_or_abort(&bars[kBarP + bx], (uint32_t)((x >> 1) & 1), abort_flag, x == 0 ? first_limit : kSpinLimit);
+      ok = wait_or_abort(&bars[kBarP + bx], (uint32_t)((x >> 1) & 1), abort_flag, x == 0 ? first_limit : kSpinLimit) &&
+           (x < kOBufs || wait_or_abort(&bars[kBarOEmpty + ob], (uint32_t)(((x - kOBufs) / kOBufs) & 1), abort_flag));
       if (!ok) break;
       const bool wide = (ref_s[(x % kRefRing) * 8 + 4] & 1u) != 0u;
       const uint32_t idesc = wide ? kIdescPVbf16 : kIdescPV;
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
               for (int hl = 0; hl < 2; ++hl) {
                 const uint64_t da = smem_desc(vbase + (2 * ks) * kVpLbo + (16 * mb) * 128, kVpLbo, 128);
                 const uint64_t db = smem_desc(pbase + hl * kPHalf + (4 * j + 2 * ks) * kPLbo, kPLbo, 128);
-                mma_pv(tmem + kColO + mb * 16, da, db, idesc, (x | j | ks | hl) != 0);
+                mma_pv(tmem + kColO + ob * 64 + mb * 16, da, db, idesc, (j | ks | hl) != 0);
               }
           commit(&bars[kBarVpEmpty + vb]);
           if (j == kSubs - 1) commit(&bars[kBarPv + ob]);
@@ -598,21 +600,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     if (!ok && lane == 0) *abort_flag = 1;
   } else if (w == kStatWarp) {
     // ================================================================ statistics
-    // Chunk c's group references E (each group's running largest visible
-    // exponent, chunks 0 .. c), whether one of them rose with this chunk, and
-    // its wide flag (a visible nonzero exponent more than 23 binades below its
-    // group's reference) into reference slot c % 4, once slot c % 4's last
-    // readers are done: P.V of chunk c - 3 finished implies that chunk c - 4's
-    // P.V and converters, and the softmax step of chunk c - 3 (which reads
-    // chunk c - 4's references as the old ones), are done.  Lane l: tokens
-    // 4l .. 4l + 3.
+    // Chunk c's group references E (each group's largest visible exponent)
+    // and its wide flag (a visible nonzero exponent more than 23 binades below
+    // its group's maximum) into reference slot c % 4, once slot c % 4's last
+    // reader, the fold of chunk c - 4, is done.  Lane l: tokens 4l .. 4l + 3.
     bool ok = true;
-    uint32_t erun[4] = {0u, 0u, 0u, 0u};
     for (int c = 0; c < n_chunks && ok; ++c) {
       const int st = c % kStages, rx = c % kRefRing;
       ok = wait_or_abort(&bars[kBarFull + st], (uint32_t)((c / kStages) & 1), abort_flag,
                          c == 0 ? first_limit : kSpinLimit) &&
-           (c < 3 || wait_or_abort(&bars[kBarPv + (c - 3) % kOBufs], (uint32_t)(((c - 3) / kOBufs) & 1), abort_flag));
+           (c < kRefRing ||
+            wait_or_abort(&bars[kBarOEmpty + (c - kRefRing) % kOBufs], (uint32_t)(((c - kRefRing) / kOBufs) & 1),
+                          abort_flag));
       if (!ok) break;
       const int pg = p0 + c * kChunkPages;
       uint32_t mx[4] = {0u, 0u, 0u, 0u}, mn[4] = {~0u, ~0u, ~0u, ~0u};
@@ -638,17 +637,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
           mn[q] = __vminu4(mn[q], __shfl_xor_sync(0xffffffffu, mn[q], o2));
         }
       if (lane == 0) {
-        uint32_t wd = 0u, up = 0u;
+        uint32_t wd = 0u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t en = __vmaxu4(erun[q], mx[q]);
-          up |= __vcmpgtu4(en, erun[q]);
-          erun[q] = en;
-          ref_s[rx * 8 + q] = en;
-          wd |= __vcmpgtu4(__vsubus4(en, mn[q]), 0x17171717u);
+          ref_s[rx * 8 + q] = mx[q];
+          wd |= __vcmpgtu4(__vsubus4(mx[q], mn[q]), 0x17171717u);
         }
         ref_s[rx * 8 + 4] = wd != 0u ? 1u : 0u;
-        ref_s[rx * 8 + 5] = up != 0u ? 1u : 0u;
         mbar_arrive(&bars[kBarRefStats + rx]);
       }
       __syncwarp();
@@ -696,6 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     const int m = 32 * w + lane;  // token of the chunk
     uint32_t* xchu = reinterpret_cast<uint32_t*>(smem + kOffXch);         // [4 warps][16]
     float* xch = reinterpret_cast<float*>(smem + kOffXch) + kSmWarps * 16;  // [4 warps][16]
+    float* alpha_s = xch + kSmWarps * 16;                                  // [3][16]
     bool ok = true;
 
     // Chunk x's scale bytes (this thread's token) as the scales of A, into
@@ -801,26 +797,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       for (int r = 0; r < kRows; ++r) o[mb][r] = 0.0f;
     int Rg[4] = {0, 0, 0, 0};  // running reference exponent of group 4 mb + w
 
-    // The accumulated O^T after the last chunk's P.V (this thread's channels)
-    // and the last chunk's group references.
-    auto fold_last = [&]() -> bool {
-      const int x = n_chunks - 1;
+    // Fold O^T of chunk x (its references in slot x % 4, its softmax
+    // factors in alpha_s[x % 3]) into the running O.
+    auto fold = [&](int x) -> bool {
+      const int ob = x % kOBufs;
+      const float* al = alpha_s + ob * kRows;
       const uint32_t* Ex = ref_s + (x % kRefRing) * 8;
-      if (!wait_or_abort(&bars[kBarPv + x % kOBufs], (uint32_t)((x / kOBufs) & 1), abort_flag)) return false;
+      if (!wait_or_abort(&bars[kBarPv + ob], (uint32_t)((x / kOBufs) & 1), abort_flag)) return false;
       fence_after_sync();
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
+      for (int hb = 0; hb < 2; ++hb) {  // channel blocks 2hb, 2hb + 1 (32 columns)
         uint32_t v[32];
-        tmem_ld32(tmem_lane + kColO + 32 * hb, v);
+        tmem_ld32(tmem_lane + kColO + ob * 64 + 32 * hb, v);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int mb = 2 * hb + i, g = 4 * mb + w;
-          Rg[mb] = (int)((Ex[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+          const int ex = (int)((Ex[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+          float gf = 1.0f, cf = 1.0f;
+          if (ex > Rg[mb]) {
+            gf = pow2_diff((uint32_t)Rg[mb], ex);
+            Rg[mb] = ex;
+          } else {
+            cf = pow2_diff((uint32_t)ex, Rg[mb]);
+          }
 #pragma unroll
-          for (int r = 0; r < kRows; ++r) o[mb][r] = __uint_as_float(v[16 * i + r]);
+          for (int r = 0; r < kRows; ++r)
+            o[mb][r] = fmaf(o[mb][r], al[r] * gf, __uint_as_float(v[16 * i + r]) * cf);
         }
       }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarOEmpty + ob]);
       return true;
     };
 
@@ -828,13 +836,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     // (the abort flag ends every other wait at once) and the next barrier,
     // where all four warps take part, turns it into a common exit.
     ok = place_sfa(0, true);
-    if (n_chunks > 1) ok = place_sfa(1, ok);
     ok = publish_ref(0, ok);
     ok = !bar_or(1, kSmWarps * 32, !ok);
     bool good = true;
     for (int c = 0; c < n_chunks && ok; ++c) {
       const int st = c % kStages, bb = c & 1;
       // ---- scales of A for chunk c + 1 (its Q.K^T runs while this chunk's softmax does)
+      if (c + 1 < n_chunks) good = place_sfa(c + 1, good);
       // ---- logits of this token: column 16i + r holds term pairs (2p + i) of row r
       good = good && wait_or_abort(&bars[kBarSFull + bb], (uint32_t)((c >> 1) & 1), abort_flag);
       if (!good && lane == 0) *abort_flag = 1;
@@ -875,10 +883,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       }
       // from here to the next barrier a failed wait only skips work
       over = xchu[8] | xchu[16 + 8] | xchu[32 + 8] | xchu[48 + 8];
-      // this chunk's factors 2^(m_old - m_new), the same in every thread
-      float alv[kRows];
+      // this chunk's factors 2^(m_old - m_new), the same in every thread: one
+      // thread keeps them for the fold (read after the next barrier)
+      const int ab = c % kOBufs;
+      if (m == 0)
 #pragma unroll
-      for (int r = 0; r < kRows; ++r) alv[r] = 1.0f;
+        for (int r = 0; r < kRows; ++r) alpha_s[ab * kRows + r] = 1.0f;
       if (over != 0u) {
         // chunk maxima of the rows that moved (rare: the first chunks and
         // jumps of more than 8)
@@ -903,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
           const float al = ex2(m_run[r] - M);
           m_run[r] = M;
           l_part[r] *= al;
-          alv[r] = al;
+          if (m == 0) alpha_s[ab * kRows + r] = al;
         }
         bar_or(1, kSmWarps * 32, false);  // the maxima are read before the next chunk's writes
       }
@@ -912,39 +922,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       for (int r = 0; r < kRows; ++r) {
         p[r] = ex2(sc[r] - m_run[r]);
         l_part[r] += p[r];
-      }
-      // ---- O^T accumulates in tensor memory over the chunks.  When a row's
-      // softmax reference or a group's V reference moved with this chunk, the
-      // accumulated O^T is rescaled in place (this thread's channel 128 mb +
-      // 32 w + lane, all rows) once P.V of chunk c - 1 is done, before P^T of
-      // this chunk releases its P.V.
-      const bool raised = c > 0 && ref_s[(c % kRefRing) * 8 + 5] != 0u;
-      if (good && c > 0 && (over != 0u || raised)) {
-        good = wait_or_abort(&bars[kBarPv + (c - 1) % kOBufs], (uint32_t)(((c - 1) / kOBufs) & 1), abort_flag);
-        if (good) {
-          fence_after_sync();
-          const uint32_t* Eo = ref_s + ((c - 1) % kRefRing) * 8;
-          const uint32_t* En = ref_s + (c % kRefRing) * 8;
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {  // channel blocks 2hb, 2hb + 1 (32 columns)
-            uint32_t v[32];
-            tmem_ld32(tmem_lane + kColO + 32 * hb, v);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int g = 4 * (2 * hb + i) + w;
-              const uint32_t eo = (Eo[g >> 2] >> (8 * (g & 3))) & 0xFFu;
-              const uint32_t en = (En[g >> 2] >> (8 * (g & 3))) & 0xFFu;
-              const float gf = en > eo ? pow2_diff(eo, (int)en) : 1.0f;
-#pragma unroll
-              for (int r = 0; r < kRows; ++r)
-                v[16 * i + r] = __float_as_uint(__uint_as_float(v[16 * i + r]) * (alv[r] * gf));
-            }
-            tmem_st32(tmem_lane + kColO + 32 * hb, v);
-          }
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          fence_before_sync();
-        }
       }
       // ---- P^T of the chunk (buffer c % 2, free once P.V of chunk c - 2 ran):
       // B-row r, token m: row octet r / 8, token octet m / 8
@@ -977,9 +954,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
       if (good && lane == 0) mbar_arrive(&bars[kBarP + bb]);
       // ---- V factors of chunk c + 1 (the converters start on it)
       if (c + 1 < n_chunks) good = publish_ref(c + 1, good);
-      // ---- scales of A for chunk c + 2 (buffer c % 2: Q.K^T of chunk c is
-      // done), so its Q.K^T runs while chunk c + 1's softmax does
-      if (c + 2 < n_chunks) good = place_sfa(c + 2, good);
+      // ---- fold chunk c - 2 (its P.V finished before P^T of chunk c went in)
+      if (good && c >= 2) good = fold(c - 2);
       if (!good && lane == 0) *abort_flag = 1;
     }
     ok = ok && good;
@@ -987,7 +963,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(DecodeArgs a
     // this barrier; then the row sums over the 128 tokens and this thread's
     // channels
     if (!bar_or(1, kSmWarps * 32, !ok)) {
-      ok = fold_last();
+      if (n_chunks >= 2) ok = fold(n_chunks - 2);
+      ok = ok && fold(n_chunks - 1);
       if (!ok && lane == 0) *abort_flag = 1;
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
